@@ -1,0 +1,295 @@
+"""ctypes wrapper around the CPU oracle (TEST INFRASTRUCTURE ONLY).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg import
+this package.  The CUDA library never does, and nothing here imports the CUDA library.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+from . import build as _build
+
+ORC_TALKER, ORC_CODEC = 0, 1
+INVALID_POS = 0xFFFFFFFF
+
+_dp = C.POINTER(C.c_double)
+_fp = C.POINTER(C.c_float)
+
+
+class OrcConfig(C.Structure):
+    _fields_ = [("kind", C.c_int), ("layers", C.c_int), ("hidden", C.c_int),
+                ("q_heads", C.c_int), ("kv_heads", C.c_int), ("head_dim", C.c_int),
+                ("inter", C.c_int), ("norm_eps", C.c_float), ("rope_theta", C.c_double),
+                ("weight_bf16", C.c_int), ("max_pos", C.c_int), ("ring", C.c_int),
+                ("window", C.c_int), ("streams", C.c_int)]
+
+
+_LAYER_FIELDS = ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown",
+                 "in_norm", "q_norm", "k_norm", "post_norm",
+                 "in_proj", "out_proj", "lin1", "lin2",
+                 "ln1_w", "ln1_b", "ln2_w", "ln2_b", "ls1", "ls2")
+
+
+class OrcLayer(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in _LAYER_FIELDS]
+
+
+_libs: Dict[str, C.CDLL] = {}
+
+
+def lib(precision: str = "f32") -> C.CDLL:
+    if precision not in _libs:
+        path = _build.lib_path(precision)
+        if not os.path.exists(path) or _build._stale(path):
+            _build.build()
+        L = C.CDLL(path)
+        L.orc_bf16_to_f32.restype = C.c_float
+        L.orc_bf16_to_f32.argtypes = [C.c_uint16]
+        L.orc_matvec_f32.argtypes = [_fp, C.c_int, C.c_int, _dp, _dp]
+        L.orc_matvec_bf16.argtypes = [C.POINTER(C.c_uint16), C.c_int, C.c_int, _dp, _dp]
+        L.orc_rms_norm.argtypes = [_dp, _fp, C.c_int, C.c_double, _dp]
+        L.orc_layer_norm.argtypes = [_dp, _fp, _fp, C.c_int, C.c_double, _dp]
+        L.orc_rope_table.argtypes = [C.c_int, C.c_double, C.c_int, _dp, _dp]
+        L.orc_mrope_table.argtypes = [C.c_int, C.c_double, C.POINTER(C.c_int),
+                                      C.POINTER(C.c_int), _dp, _dp]
+        L.orc_rope_rotate_half.argtypes = [_dp, C.c_int, _dp, _dp]
+        L.orc_rope_interleaved.argtypes = [_dp, C.c_int, _dp, _dp]
+        L.orc_silu.restype = C.c_double
+        L.orc_silu.argtypes = [C.c_double]
+        L.orc_gelu.restype = C.c_double
+        L.orc_gelu.argtypes = [C.c_double]
+        L.orc_gqa_attention.argtypes = [_dp, _dp, _dp, C.c_int, C.c_int, C.c_int, C.c_int, _dp]
+        L.orc_ring_attention.argtypes = [_dp, _dp, _dp, C.POINTER(C.c_uint32), C.c_int,
+                                         C.c_int, C.c_uint32, C.c_int, C.c_int, _dp]
+        L.orc_create.restype = C.c_void_p
+        L.orc_create.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcLayer), _fp]
+        L.orc_prefill_kv.argtypes = [C.c_void_p, C.c_int, _fp, _fp, C.c_int]
+        L.orc_step.argtypes = [C.c_void_p, C.c_int, _fp, C.POINTER(C.c_int), _dp, _dp]
+        L.orc_reset.argtypes = [C.c_void_p, C.c_int]
+        L.orc_len.argtypes = [C.c_void_p, C.c_int]
+        L.orc_read_kv.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, _dp, _dp]
+        L.orc_destroy.argtypes = [C.c_void_p]
+        L.orc_set_threads.argtypes = [C.c_int]
+        L.orc_get_threads.restype = C.c_int
+        _libs[precision] = L
+    return _libs[precision]
+
+
+def _d(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray, ct):
+    return a.ctypes.data_as(C.POINTER(ct))
+
+
+# ---------------------------------------------------------------------------- primitives
+
+def bf16_to_f32(bits: int, precision: str = "f32") -> float:
+    return float(lib(precision).orc_bf16_to_f32(int(bits)))
+
+
+def matvec(W: np.ndarray, x, precision: str = "f32") -> np.ndarray:
+    """y = W x, W row-major [N][K] float32 or uint16 (bf16 bits)."""
+    W = np.ascontiguousarray(W)
+    N, K = W.shape
+    x = _d(x)
+    y = np.empty(N, np.float64)
+    if W.dtype == np.uint16:
+        lib(precision).orc_matvec_bf16(_ptr(W, C.c_uint16), N, K, _ptr(x, C.c_double),
+                                       _ptr(y, C.c_double))
+    else:
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        lib(precision).orc_matvec_f32(_ptr(W, C.c_float), N, K, _ptr(x, C.c_double),
+                                      _ptr(y, C.c_double))
+    return y
+
+
+def rms_norm(x, w, eps: float, precision: str = "f32") -> np.ndarray:
+    x = _d(x)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    y = np.empty_like(x)
+    lib(precision).orc_rms_norm(_ptr(x, C.c_double), _ptr(w, C.c_float), x.size, eps,
+                                _ptr(y, C.c_double))
+    return y
+
+
+def layer_norm(x, w, b, eps: float, precision: str = "f32") -> np.ndarray:
+    x = _d(x)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    y = np.empty_like(x)
+    lib(precision).orc_layer_norm(_ptr(x, C.c_double), _ptr(w, C.c_float), _ptr(b, C.c_float),
+                                  x.size, eps, _ptr(y, C.c_double))
+    return y
+
+
+def rope_table(d: int, theta: float, pos: int, precision: str = "f32"):
+    c = np.empty(d // 2, np.float64)
+    s = np.empty(d // 2, np.float64)
+    lib(precision).orc_rope_table(d, theta, pos, _ptr(c, C.c_double), _ptr(s, C.c_double))
+    return c, s
+
+
+def mrope_table(d: int, theta: float, pos3: Sequence[int], assign: Sequence[int],
+                precision: str = "f32"):
+    p = np.ascontiguousarray(pos3, dtype=np.int32)
+    a = np.ascontiguousarray(assign, dtype=np.int32)
+    c = np.empty(d // 2, np.float64)
+    s = np.empty(d // 2, np.float64)
+    lib(precision).orc_mrope_table(d, theta, _ptr(p, C.c_int), _ptr(a, C.c_int),
+                                   _ptr(c, C.c_double), _ptr(s, C.c_double))
+    return c, s
+
+
+def rope_rotate_half(x, c, s, precision: str = "f32") -> np.ndarray:
+    x = _d(x).copy()
+    c, s = _d(c), _d(s)
+    lib(precision).orc_rope_rotate_half(_ptr(x, C.c_double), x.size, _ptr(c, C.c_double),
+                                        _ptr(s, C.c_double))
+    return x
+
+
+def rope_interleaved(x, c, s, precision: str = "f32") -> np.ndarray:
+    x = _d(x).copy()
+    c, s = _d(c), _d(s)
+    lib(precision).orc_rope_interleaved(_ptr(x, C.c_double), x.size, _ptr(c, C.c_double),
+                                        _ptr(s, C.c_double))
+    return x
+
+
+def silu(g: float, precision: str = "f32") -> float:
+    return lib(precision).orc_silu(float(g))
+
+
+def gelu(v: float, precision: str = "f32") -> float:
+    return lib(precision).orc_gelu(float(v))
+
+
+def gqa_attention(q, kc, vc, precision: str = "f32") -> np.ndarray:
+    """q [H][d]; kc, vc [L][G][d] position-major -> out [H][d]."""
+    q = _d(q)
+    kc = _d(kc)
+    vc = _d(vc)
+    H, d = q.shape
+    L, G, _ = kc.shape
+    out = np.empty((H, d), np.float64)
+    lib(precision).orc_gqa_attention(_ptr(q, C.c_double), _ptr(kc, C.c_double),
+                                     _ptr(vc, C.c_double), L, H, G, d, _ptr(out, C.c_double))
+    return out
+
+
+def ring_attention(q, kr, vr, pr, window: int, pos: int, precision: str = "f32") -> np.ndarray:
+    """q [H][d]; kr, vr [ring][H][d]; pr [ring] uint32 stamps -> out [H][d]."""
+    q = _d(q)
+    kr = _d(kr)
+    vr = _d(vr)
+    pr = np.ascontiguousarray(pr, dtype=np.uint32)
+    H, d = q.shape
+    ring = kr.shape[0]
+    out = np.empty((H, d), np.float64)
+    lib(precision).orc_ring_attention(_ptr(q, C.c_double), _ptr(kr, C.c_double),
+                                      _ptr(vr, C.c_double), _ptr(pr, C.c_uint32), ring, window,
+                                      pos, H, d, _ptr(out, C.c_double))
+    return out
+
+
+def set_threads(n: int) -> None:
+    for p in ("f32", "f64"):
+        lib(p).orc_set_threads(int(n))
+
+
+# ---------------------------------------------------------------------------- the stack
+
+class OracleModel:
+    """The decode stack on the CPU, holding its own K/V state.
+
+    ``syn`` is a :class:`tts_autoregressive_decode_gb300.workloads.Synthetic` (or anything
+    with the same fields); the weight arrays are referenced, not copied.
+    """
+
+    def __init__(self, syn, precision: str = "f32", threads: Optional[int] = None):
+        w = syn.workload
+        self.w = w
+        self.precision = precision
+        self.L = lib(precision)
+        if threads is not None:
+            self.L.orc_set_threads(int(threads))
+        cfg = OrcConfig(kind=ORC_TALKER if w.kind == "talker" else ORC_CODEC,
+                        layers=w.layers, hidden=w.hidden, q_heads=w.q_heads,
+                        kv_heads=w.kv_heads, head_dim=w.head_dim, inter=w.inter,
+                        norm_eps=w.norm_eps, rope_theta=w.rope_theta,
+                        weight_bf16=1 if w.weight_dtype == "bf16" else 0,
+                        max_pos=syn.max_pos, ring=w.ring, window=w.window, streams=w.streams)
+        self._keep: List[np.ndarray] = []
+        arr = (OrcLayer * w.layers)()
+        for i, d in enumerate(syn.layers):
+            for name, a in d.items():
+                a = np.ascontiguousarray(a)
+                self._keep.append(a)
+                setattr(arr[i], name, a.ctypes.data)
+        fn = None
+        if syn.final_norm is not None:
+            fn_arr = np.ascontiguousarray(syn.final_norm, dtype=np.float32)
+            self._keep.append(fn_arr)
+            fn = _ptr(fn_arr, C.c_float)
+        self._layers = arr
+        self._cfg = cfg
+        self.h = self.L.orc_create(C.byref(cfg), arr, fn)
+        if not self.h:
+            raise ValueError("oracle rejected the configuration")
+        for s, n in enumerate(syn.lengths):
+            if n > 0:
+                self.prefill_kv(s, syn.prefill_k[s], syn.prefill_v[s])
+
+    def prefill_kv(self, stream: int, k: np.ndarray, v: np.ndarray) -> None:
+        k = np.ascontiguousarray(k, dtype=np.float32)
+        v = np.ascontiguousarray(v, dtype=np.float32)
+        rc = self.L.orc_prefill_kv(self.h, stream, _ptr(k, C.c_float), _ptr(v, C.c_float),
+                                   k.shape[1])
+        if rc != 0:
+            raise ValueError(f"orc_prefill_kv failed ({rc})")
+
+    def step(self, x_in: np.ndarray, pos: Sequence[int], taps: bool = False):
+        x_in = np.ascontiguousarray(x_in, dtype=np.float32)
+        rows = x_in.shape[0]
+        p = np.ascontiguousarray(pos, dtype=np.int32)
+        out = np.empty((rows, self.w.hidden), np.float64)
+        t = np.empty((self.w.layers, rows, self.w.hidden), np.float64) if taps else None
+        rc = self.L.orc_step(self.h, rows, _ptr(x_in, C.c_float), _ptr(p, C.c_int),
+                             _ptr(out, C.c_double), _ptr(t, C.c_double) if taps else None)
+        if rc != 0:
+            raise ValueError(f"orc_step failed ({rc})")
+        return (out, t) if taps else out
+
+    def length(self, stream: int) -> int:
+        return int(self.L.orc_len(self.h, stream))
+
+    def read_kv(self, layer: int, stream: int, pos: int):
+        n = self.w.kv_heads * self.w.head_dim
+        k = np.empty(n, np.float64)
+        v = np.empty(n, np.float64)
+        rc = self.L.orc_read_kv(self.h, layer, stream, pos, _ptr(k, C.c_double),
+                                _ptr(v, C.c_double))
+        if rc != 0:
+            raise ValueError("orc_read_kv failed")
+        return (k.reshape(self.w.kv_heads, self.w.head_dim),
+                v.reshape(self.w.kv_heads, self.w.head_dim))
+
+    def reset(self, stream: int) -> None:
+        self.L.orc_reset(self.h, stream)
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            self.L.orc_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
