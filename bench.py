@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one decode step of the whole layer stack (every kernel of the plan) over one batch of
+synthetic input resident in HBM.  The default workload is the 28-layer bf16 talker (h2048,
+16/8 heads, d128, SwiGLU 6144) with 2048 prefilled positions; its 128-step position range
+2048..2175 is replayed cyclically (the stream is truncated back to 2048 after every 128 steps),
+so every timed step is a genuine step of that workload.  Its per-step working set (3.3 GB of
+weights and KV) is far larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path has no
+exchange step); the timed region is bracketed by barriers, the time is the max over ranks and
+the value is the aggregate steps/s of all ranks.
+
+--impl reference times the CPU oracle (the plain sequential C restatement) on the host cores
+with the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tts_autoregressive_decode_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode steps/sec and achieved HBM GB/s (% of GB300 peak) per token, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the dominant kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), with the hash of the kernel source it was taken on.  A changed kernel
+# reports null until it is captured again.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1280)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=W.TALKER_H2048_L28.name,
+                   choices=sorted(W.WORKLOADS))
+    p.add_argument("--kernel-rounds", type=int, default=3)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured hbm_gbs (MEASURED_PEAKS.json, STREAM-style copy)"
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+# ------------------------------------------------------------------------------ bytes
+
+def vector_bytes(w: W.Workload) -> int:
+    h, d = w.hidden, w.head_dim
+    per = (2 * h + 2 * d) if w.kind == "talker" else 6 * h
+    return 4 * (w.layers * per + (h if w.kind == "talker" else 0))
+
+
+def kv_bytes(w: W.Workload, positions) -> int:
+    """K and V bytes a step reads: talker pos+1 keys per stream and layer; codec: the ring."""
+    if w.kind == "talker":
+        return sum(2 * (p + 1) * w.kvw * 4 * w.layers for p in positions)
+    return len(positions) * w.layers * (2 * w.ring * w.hidden * 4 + 4 * w.ring)
+
+
+def step_bytes(w: W.Workload, positions) -> int:
+    return w.matrix_bytes() + vector_bytes(w) + kv_bytes(w, positions)
+
+
+def dominant_kernel(w: W.Workload, m: int):
+    """(stage, name, algorithmic bytes per launch) of the plan's largest kernel."""
+    es = 2 if w.weight_dtype == "bf16" else 4
+    h, I = w.hidden, w.inter
+    if w.kind == "talker":
+        return (3, "norm + gate/up GEMV + SwiGLU (k_gemv)",
+                2 * I * h * es + 4 * (m * h + h + m * I))
+    return (3, "LayerNorm + lin1 GEMV + GELU (k_gemv)", I * h * es + 4 * (m * h + 2 * h + m * I))
+
+
+def kernel_source_sha() -> str:
+    src = os.path.join(ROOT, "tts_autoregressive_decode_gb300", "csrc", "gemv.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------ oracle timing
+
+def oracle_rate(syn, seconds: float, threads: int, max_steps: int = 64, layers=None):
+    """Steps/s of the CPU oracle on the workload's first steps (a bounded sample)."""
+    import oracle
+
+    w = syn.workload
+    if layers is not None and layers < w.layers:
+        import dataclasses
+        sub = dataclasses.replace(syn, workload=dataclasses.replace(w, layers=layers),
+                                  layers=syn.layers[:layers],
+                                  prefill_k=[None if k is None else k[:layers] for k in syn.prefill_k],
+                                  prefill_v=[None if v is None else v[:layers] for v in syn.prefill_v])
+        syn = sub
+    orc = oracle.OracleModel(syn, threads=threads)
+    m = w.streams
+    t0 = time.perf_counter()
+    n = 0
+    x = syn.x0 if w.feedback else None
+    while n < max_steps and (n == 0 or time.perf_counter() - t0 < seconds):
+        t = n % w.steps
+        if n and t == 0:
+            for s in range(m):
+                orc.prefill_kv(s, syn.prefill_k[s], syn.prefill_v[s]) if syn.lengths[s] else orc.reset(s)
+        xin = x if w.feedback else syn.inputs[t]
+        y = orc.step(xin, [orc.length(s) for s in range(m)])
+        if w.feedback:
+            x = (y.astype(np.float32) + syn.e).astype(np.float32)
+        n += 1
+    dt = time.perf_counter() - t0
+    orc.close()
+    return n, dt
+
+
+# ------------------------------------------------------------------------------ arms
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    syn = W.generate(w)
+    threads = os.cpu_count() or 1
+    # one full step first, to size the per-step sample so the whole run stays within minutes
+    n1, dt1 = oracle_rate(syn, 0.0, threads, max_steps=1)
+    budget = 150.0
+    layers = w.layers
+    if (args.steps + args.warmup) * dt1 > budget:
+        layers = max(1, int(w.layers * budget / ((args.steps + args.warmup) * dt1)))
+    _, _ = oracle_rate(syn, 1e9, threads, max_steps=args.warmup, layers=layers) if args.warmup else (0, 0)
+    n, dt = oracle_rate(syn, 1e9, threads, max_steps=args.steps, layers=layers)
+    per_step = dt / n * (w.layers / layers)       # full-stack equivalent seconds per step
+    value = 1.0 / per_step
+    sample = (f"{n} steps of the {w.layers}-layer workload"
+              + (f", each timed on its first {layers} layers and scaled by {w.layers}/{layers}"
+                 if layers < w.layers else "")
+              + f", positions from the workload start, {threads} threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "streams": w.streams},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args):
+    import torch
+
+    from tts_autoregressive_decode_gb300 import native_build
+    from tts_autoregressive_decode_gb300.decoder import Decoder
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    if rank == 0 or world == 1:
+        native_build.build()
+    if pg:
+        pg.barrier()
+    w = W.WORKLOADS[args.workload]
+    talker = w.kind == "talker"
+    syn = W.generate(w)
+    if not talker:
+        # the ring keeps positions growing: size the RoPE table for warm-up + timed + e2e steps
+        syn.max_pos = max(syn.max_pos, 2 * (args.warmup + args.steps) + 2 * w.steps + 8)
+    dec = Decoder.from_synthetic(syn)
+    m, h = w.streams, w.hidden
+    base = list(syn.lengths)
+    X = torch.from_numpy(syn.inputs).cuda()                  # [steps][m][h], resident in HBM
+    out = torch.empty((m, h), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    set_len_kernels = [0]
+
+    def positions(i):
+        return [b + (i % w.steps) for b in base] if talker else [dec.length(s) for s in range(m)]
+
+    def one_step(i, x=None):
+        t = i % w.steps
+        if talker and t == 0 and dec.length(0) != base[0]:
+            for s in range(m):
+                dec.truncate(s, base[s])
+            set_len_kernels[0] += m
+        dec.step(X[t] if x is None else x, dec.lengths(m), out)
+
+    # ---- warm-up, then rewind to the workload's first position -----------------------------
+    for i in range(args.warmup):
+        one_step(i)
+    dec.sync()
+    if talker:
+        for s in range(m):
+            dec.truncate(s, base[s])
+    dec.sync()
+    pos_before = dec.lengths(m)
+
+    # ---- timed region: K steps, CUDA events on the launching stream -------------------------
+    step_positions = [positions(i) if talker else None for i in range(min(args.steps, w.steps))]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    set_len_kernels[0] = 0
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        one_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    dec.sync()
+    ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    launches = args.steps * dec.kernels_per_step(m) + set_len_kernels[0]
+
+    # bytes: mean over the steps actually timed (the talker's range cycles)
+    if talker:
+        per_cycle = [step_bytes(w, p) for p in step_positions]
+        nb = sum(per_cycle[i % len(per_cycle)] for i in range(args.steps)) / args.steps
+    else:
+        nb = step_bytes(w, [0] * m)
+    ms_step = ms / args.steps
+    value = world * args.steps / (ms / 1e3)
+    peak, peak_src = peaks()
+    step_gbs = nb / (ms_step * 1e-3) / 1e9
+
+    # ---- dominant kernel on its own: one launch per layer, CUDA events around each ----------
+    stage, kname, kbytes = dominant_kernel(w, m)
+    durs = []
+    for _ in range(args.kernel_rounds):
+        evs = []
+        for l in range(w.layers):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dec.launch_stage(l, stage, m)
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        durs += [a.elapsed_time(b) for a, b in evs]
+    k_ms = sum(durs) / len(durs)
+    k_gbs = kbytes / (k_ms * 1e-3) / 1e9
+    sha = kernel_source_sha()
+    tr = NCU_TRAFFIC.get(w.name)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("source_sha") == sha else None
+
+    # ---- end to end through the C ABI with host buffers ----------------------------------------
+    e2e = None
+    if not args.no_e2e:
+        if talker:
+            for s in range(m):
+                dec.truncate(s, base[s])
+        xh = torch.from_numpy(syn.inputs.copy()).pin_memory()
+        oh = torch.empty((m, h), dtype=torch.float32).pin_memory()
+        import ctypes as C
+        dec.sync()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            t = i % w.steps
+            if talker and t == 0 and dec.length(0) != base[0]:
+                for s in range(m):
+                    dec.truncate(s, base[s])
+            p = (C.c_int32 * m)(*dec.lengths(m))
+            dec.step_host_ptr(m, xh[t].data_ptr(), p, oh.data_ptr())
+        dt = time.perf_counter() - t0
+        if pg:
+            t = torch.tensor([dt], device="cuda")
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * args.steps / dt, "unit": "steps/s",
+               "h2d_bytes_per_step": m * h * 4, "d2h_bytes_per_step": m * h * 4 + 4}
+
+    # ---- the oracle on the host cores (rank 0, one GPU only) -----------------------------------
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        threads = os.cpu_count() or 1
+        n, dt = oracle_rate(syn, args.cpu_seconds, threads)
+        cpu = {"value": n / dt, "unit": "steps/s", "cores": threads, "kind": "oracle",
+               "sample": f"the first {n} steps of {w.name} (positions from the workload start), "
+                         f"{dt:.1f} s on {threads} threads"}
+
+    if rank != 0:
+        return
+    cfg = {"workload": w.name, "layers": w.layers, "hidden": w.hidden,
+           "heads": f"{w.q_heads}/{w.kv_heads}", "head_dim": w.head_dim, "inter": w.inter,
+           "weights": w.weight_dtype, "kv": "f32", "streams": m,
+           "positions": (f"{pos_before}..+{w.steps - 1}, replayed cyclically" if talker
+                         else f"from {pos_before}, continuing"),
+           "l2": ("no flush: per-step working set %.2f GB >> 129 MB L2" % (nb / 1e9)
+                  if nb > 4 * 129e6 else
+                  "per-step working set %.1f MB may be partly L2-resident" % (nb / 1e6)),
+           "graph": "one CUDA graph per step, 5 PDL-chained kernels per layer + 1",
+           "parallelism": f"replicas x{world}"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": cfg,
+        "tokens_per_s": value * m,
+        "achieved_hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak,
+        "bytes_per_step": nb,
+        "roofline": {"bound": "hbm", "achieved": k_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": k_gbs / peak, "traffic": traffic, "kernel": kname,
+                     "bytes_per_launch": kbytes, "us_per_launch": k_ms * 1e3,
+                     "peak_source": peak_src + " (burst: kernel timed alone)"},
+        "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                          "frac": step_gbs / peak, "bytes_per_step": nb},
+        "gpu_launches": launches,
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+    }
+    print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

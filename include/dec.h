@@ -1,0 +1,240 @@
+/*
+ * dec.h -- C ABI of the GB300 (sm_103a) single-token autoregressive decode library.
+ *
+ * One call of dec_step advances m independent decode streams by one position through a
+ * stack of transformer layers of one of two kinds:
+ *
+ *   DEC_QWEN3_TALKER   the Qwen3-style TTS talker layer (Qwen3-TTS talker on wgpu,
+ *                      inferencelayer qwen3tts_gpu.rs, build_step_plan): RMSNorm, q/k/v
+ *                      row-major GEMVs, per-head q/k RMSNorm, 1-D rotate_half RoPE, KV
+ *                      append, causal GQA attention over the whole cache, o-proj + residual,
+ *                      RMSNorm, gate/up GEMVs + SwiGLU, down-proj + residual; final RMSNorm.
+ *   DEC_CODEC_WINDOWED the codec-style layer over a KV ring (Mimi on wgpu, inferencelayer
+ *                      mimi_gpu.rs, transformer_shaped): LayerNorm, qkv GEMV, interleaved
+ *                      RoPE + ring push + position stamp, windowed attention, out-proj with
+ *                      LayerScale residual, LayerNorm, lin1 + GELU(erf), lin2 with LayerScale
+ *                      residual; the output is the residual stream (no final norm).
+ *
+ * Every step of the path runs in this library's CUDA kernels.  Pointers are plain host or
+ * device addresses as stated per argument; `void* stream` is a cudaStream_t (0 = legacy
+ * default stream).  Sizes are in elements unless they say bytes.  All functions return a
+ * dec_status; on failure dec_last_error(ctx) holds a one-line reason and the context's
+ * state is unchanged, except for DEC_E_CUDA / DEC_E_DEVICE_CHECK, after which the context
+ * should be destroyed.  A context is not thread-safe: one host thread at a time.
+ */
+#ifndef DEC_H
+#define DEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DEC_ABI_VERSION 1
+
+typedef enum {
+    DEC_OK = 0,
+    DEC_E_ARG = 1,          /* null pointer, out-of-range size, inconsistent configuration */
+    DEC_E_POS = 2,          /* pos[i] differs from the current length of stream i */
+    DEC_E_CAPACITY = 3,     /* a position would reach max_pos, or a prefill exceeds capacity */
+    DEC_E_UNSUPPORTED = 4,  /* a shape or dtype outside what the kernels implement */
+    DEC_E_CUDA = 5,         /* a CUDA runtime call failed (text in dec_last_error) */
+    DEC_E_DEVICE_CHECK = 6  /* a kernel's own bounds or wait-limit check fired */
+} dec_status;
+
+typedef enum { DEC_QWEN3_TALKER = 0, DEC_CODEC_WINDOWED = 1 } dec_kind;
+typedef enum { DEC_F32 = 0, DEC_BF16 = 1 } dec_dtype;
+
+/* flags */
+#define DEC_FLAG_TAPS 1u     /* keep the residual stream after every layer (dec_read_tap) */
+#define DEC_FLAG_NO_GRAPH 2u /* launch kernels one by one instead of replaying a CUDA graph */
+
+/*
+ * Model geometry.  Talker fields follow the talker's Dims (Qwen3-TTS talker on wgpu, `Dims`
+ * and load()); codec fields follow TrShape (Mimi on wgpu, `TrShape`).
+ *   hidden      h (talker) or d_model (codec); multiple of 8
+ *   q_heads     H; kv_heads G; H % G == 0 (codec: G == H and H * head_dim == hidden)
+ *   head_dim    d: 64 or 128 (the talker page bounds it by 128, load())
+ *   inter       SwiGLU width (talker) or MLP width (codec); multiple of 8
+ *   norm_eps    RMSNorm eps (talker, 1e-6) or LayerNorm eps (codec, 1e-5)
+ *   rope_theta  RoPE base: 1e6 (talker, rotate_half), 1e4 (codec, interleaved pairs)
+ *   weight_dtype storage type of every matrix: DEC_F32 or DEC_BF16 (widened to f32 exactly
+ *               in-kernel); norm weights, biases and LayerScale vectors are always f32
+ *   max_pos     talker: KV capacity per stream (a step at pos needs pos + 1 <= max_pos);
+ *               codec: positions must stay below max_pos (length of the RoPE table)
+ *   ring        codec: KV ring slots per layer and stream; window: attention window,
+ *               1 <= window <= ring (window == ring means unbounded within the ring)
+ *   max_streams number of decode streams (rows) the context holds state for: 1..8
+ */
+typedef struct {
+    int32_t kind;          /* dec_kind */
+    int32_t layers;
+    int32_t hidden;
+    int32_t q_heads;
+    int32_t kv_heads;
+    int32_t head_dim;
+    int32_t inter;
+    float norm_eps;
+    double rope_theta;
+    int32_t weight_dtype;  /* dec_dtype */
+    int32_t max_pos;
+    int32_t ring;
+    int32_t window;
+    int32_t max_streams;
+    uint32_t flags;        /* DEC_FLAG_* */
+} dec_config;
+
+/*
+ * Per-layer weights: DEVICE pointers, read only during dec_create (the library copies them
+ * into its own arena, so the caller may free them afterwards).  Matrices are row-major
+ * [out][in], exactly as a Linear stores them and as the talker page uploads them
+ * (Qwen3-TTS talker on wgpu, load(): "row-major [n,k] -- uploaded as-is"), 16-byte aligned.
+ * Talker: q [H*d][h], k [G*d][h], v [G*d][h], o [h][H*d], gate [inter][h], up [inter][h],
+ *         down [h][inter]; in_norm [h], q_norm [d], k_norm [d], post_norm [h] (f32).
+ * Codec:  in_proj [3*hidden][hidden] with rows [q | k | v], each head-major; out_proj
+ *         [hidden][hidden]; lin1 [inter][hidden]; lin2 [hidden][inter]; ln1_w, ln1_b,
+ *         ln2_w, ln2_b, ls1, ls2 [hidden] (f32).  Fields of the other kind are ignored.
+ */
+typedef struct {
+    const void *q, *k, *v, *o, *gate, *up, *down;
+    const float *in_norm, *q_norm, *k_norm, *post_norm;
+    const void *in_proj, *out_proj, *lin1, *lin2;
+    const float *ln1_w, *ln1_b, *ln2_w, *ln2_b, *ls1, *ls2;
+} dec_layer_weights;
+
+typedef struct {
+    const dec_layer_weights* layers; /* HOST array of `layers` entries */
+    const float* final_norm;         /* talker: DEVICE [h] f32; codec: ignored */
+} dec_weights;
+
+typedef struct dec_ctx dec_ctx;
+
+/* Create a context on the current CUDA device: validates the configuration, allocates the
+ * weight arena, KV caches (talker: [layers][streams][G][max_pos][d] f32; codec: rings
+ * [layers][streams][H][ring][d] f32 plus u32 position rings, all stamped empty), RoPE
+ * tables and scratch, and copies the weights.  The talker page's load() sizes the same
+ * state (Qwen3-TTS talker on wgpu, load() and new_state()).  `stream` is where every later
+ * step is enqueued.  On success *out owns all of it until dec_destroy. */
+dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream, dec_ctx** out);
+
+/* Free everything the context owns.  Waits for the context's stream first.  NULL is a no-op. */
+void dec_destroy(dec_ctx* ctx);
+
+/* One-line text of the last failure on this context (empty string if none).  With ctx ==
+ * NULL, the last failure of dec_create on this thread. */
+const char* dec_last_error(const dec_ctx* ctx);
+
+/* Replace the stream later calls enqueue on. */
+dec_status dec_set_stream(dec_ctx* ctx, void* stream);
+
+/* Load a stream's cache from prefilled keys and values, as the backbone's voice load does
+ * (Pocket TTS on wgpu, load_voice(): the stored keys already carry RoPE, so it is a copy).
+ * k, v: DEVICE [layers][n_pos][kv_heads][head_dim] f32.  The stream is reset first; then
+ * talker: cache rows 0..n_pos-1; codec: ring slots 0..n_pos-1 stamped with positions
+ * 0..n_pos-1 (n_pos <= ring).  The stream's length becomes n_pos.  Asynchronous on the
+ * context's stream; k and v must stay valid until it has run.
+ * Errors: DEC_E_ARG (stream out of range, n_pos < 0, null with n_pos > 0), DEC_E_CAPACITY
+ * (n_pos > max_pos for the talker, n_pos > ring for the codec). */
+dec_status dec_prefill_kv(dec_ctx* ctx, int stream, const float* k, const float* v, int n_pos);
+
+/* One decode step of streams 0..m-1 (Qwen3-TTS talker on wgpu, step(): the new K/V row is
+ * appended at `pos`, attention covers pos + 1 keys, the final-norm hidden is returned;
+ * Pocket TTS on wgpu, step_device(): the output stays on the device).
+ *   m           rows = streams 0..m-1, 1 <= m <= max_streams
+ *   x_in        DEVICE [m][hidden] f32, the input embeddings
+ *   pos         HOST [m]; pos[i] must equal stream i's current length (contiguous
+ *               positions, as step() demands) and pos[i] + 1 <= max_pos (talker) or
+ *               pos[i] < max_pos (codec)
+ *   hidden_out  DEVICE [m][hidden] f32: talker final-norm hidden, codec residual stream;
+ *               must not overlap x_in
+ * Asynchronous: enqueued on the context's stream, returns without waiting; x_in must not
+ * change and hidden_out must not be read until the stream reaches this point.  The first
+ * step with a given (m, x_in, hidden_out) captures a CUDA graph (milliseconds); later steps
+ * replay it.  Lengths advance by one on success; nothing changes on an error. */
+dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, float* hidden_out);
+
+/* dec_step with HOST buffers, blocking, as the talker page's step() returns its hidden state
+ * to the host (Qwen3-TTS talker on wgpu, step(): write_buffer, submit, blocking read).
+ * x_in_host [m][hidden] and hidden_out_host [m][hidden] f32 in host memory (pinned or not);
+ * copies in, runs the step, copies out and waits.  Also reports device-side check failures
+ * (DEC_E_DEVICE_CHECK) like dec_sync. */
+dec_status dec_step_host(dec_ctx* ctx, int m, const float* x_in_host, const int32_t* pos,
+                         float* hidden_out_host);
+
+/* Clear one stream: length 0, its K/V zeroed, and (codec) every position stamp set to
+ * empty by ring capacity (Mimi on wgpu, reset(); Pocket TTS on wgpu, reset()).
+ * Asynchronous on the context's stream. */
+dec_status dec_reset(dec_ctx* ctx, int stream);
+
+/* Wait for the context's stream, then read the kernels' device check word: DEC_OK, or
+ * DEC_E_DEVICE_CHECK naming the check (bounds or wait limit), or DEC_E_CUDA. */
+dec_status dec_sync(dec_ctx* ctx);
+
+/* Current length (next position) of a stream as the host sees it, or -1 on a bad index. */
+int dec_get_len(const dec_ctx* ctx, int stream);
+
+/* Copy the stored key and value of (layer, stream, position) to HOST [kv_heads][head_dim]
+ * f32 each (codec: the slot position % ring).  Synchronous.  For tests and inspection. */
+dec_status dec_read_kv(dec_ctx* ctx, int layer, int stream, int position, float* k_host,
+                       float* v_host);
+
+/* With DEC_FLAG_TAPS: copy the residual stream after `layer` of the last step to HOST
+ * [m][hidden] f32 (the pages' stage probes, Mimi on wgpu, debug_read()).  Synchronous. */
+dec_status dec_read_tap(dec_ctx* ctx, int layer, int m, float* dst_host);
+
+/* Number of CUDA kernels one step of m rows launches (for launch accounting). */
+int dec_kernels_per_step(const dec_ctx* ctx, int m);
+
+/* Talker only: shorten stream `stream` to `new_len` positions (0 <= new_len <= its length), so
+ * the next step is at position new_len.  Cache rows below new_len are kept (rows at and above
+ * it are overwritten by later steps), e.g. to roll back rejected positions or to replay a fixed
+ * position range.  Asynchronous.  Errors: DEC_E_ARG (range), DEC_E_UNSUPPORTED (codec ring:
+ * its slots are reused, so earlier positions cannot be restored). */
+dec_status dec_truncate(dec_ctx* ctx, int stream, int new_len);
+
+/* Enqueue exactly one kernel of the step plan for rows 0..m-1, on the context's stream, from
+ * the context's current buffers -- for timing a kernel on its own (the per-kernel attribution
+ * of the pages' bench_steps, Mimi on wgpu).  stage: 0 norm + q/k/v GEMV, 1 attention (with its
+ * prologue), 2 o-proj + residual, 3 norm + gate/up + SwiGLU (codec: lin1 + GELU), 4 down +
+ * residual (codec: lin2).  Layer 0's stages 0 and 2 read the context's internal input buffer.
+ * Lengths do not advance; stage 1 writes the K/V row (ring slot) of the next position, which
+ * the next step rewrites.  Not for use between a dec_step and its completion. */
+dec_status dec_launch_stage(dec_ctx* ctx, int layer, int stage, int m);
+
+/* ---------------------------------------------------------------------------------------
+ * Stateless kernel entry points (the same kernels the step uses, on caller buffers).
+ * ------------------------------------------------------------------------------------- */
+
+/* Row-major GEMV (Qwen3-TTS talker on wgpu, MATVEC_SRC): y[r][n] = sum_k W[n][k] x[r][k]
+ * for r < m, each weight read once for all m rows.
+ *   dtype  DEC_F32 or DEC_BF16 (W as bf16 bit patterns, widened exactly)
+ *   W      DEVICE [N][K], 16-byte aligned, K % 8 == 0
+ *   x      DEVICE [m][K] f32, 16-byte aligned;  y: DEVICE [m][N] f32;  1 <= m <= 8
+ * Asynchronous on `stream`.  Errors: DEC_E_ARG, DEC_E_UNSUPPORTED (K % 8, alignment). */
+dec_status dec_gemv(int dtype, const void* W, int N, int K, const float* x, int m, float* y,
+                    void* stream);
+
+/* Split-K GQA decode attention (Qwen3-TTS talker on wgpu, GQA_ATTN_SRC), one query row per
+ * stream: out[r][i] = sum_j softmax_j(q[r][i] . K[r][g][j] / sqrt(d)) V[r][g][j] over
+ * j < lens[r], with g = i / (H / G).
+ *   q      DEVICE [m][H][d] f32 (already normalised and rotated)
+ *   k, v   DEVICE [m][G][capacity][d] f32, head-major caches, 16-byte aligned
+ *   lens   DEVICE [m] int32, 1 <= lens[r] <= capacity
+ *   out    DEVICE [m][H][d] f32
+ *   workspace  DEVICE scratch of dec_attention_workspace_bytes(...) bytes, 16-byte
+ *          aligned, used for per-chunk partial results and merge tickets; its ticket words
+ *          must be zero before the first call (cudaMemset) -- every call leaves them zero
+ *          again.  Calls sharing one workspace must not overlap on the GPU.
+ * Asynchronous on `stream`.  head_dim 64 or 128, H / G <= 8, m <= 64. */
+size_t dec_attention_workspace_bytes(int m, int q_heads, int kv_heads, int head_dim,
+                                     int capacity);
+dec_status dec_attention(int m, int q_heads, int kv_heads, int head_dim, int capacity,
+                         const float* q, const float* k, const float* v, const int32_t* lens,
+                         float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DEC_H */

@@ -1,0 +1,384 @@
+// attention.cu -- split-K decode attention with the step's q/k prologue fused in (sm_103a).
+//
+// One CTA per (key chunk c, kv head g, stream r).  It serves every q head of the GQA group of g
+// (kv head of q head i is i / (H/G), Qwen3-TTS talker on wgpu, GQA_ATTN_SRC), so each K/V
+// element is read from HBM once per step.  The chunk's cached K and V rows (64 keys, head-major
+// cache, contiguous) are staged into shared memory by two 1-D bulk copies (cp.async.bulk) on an
+// mbarrier; they are issued BEFORE griddepcontrol.wait because cached rows never change during
+// the step.
+//
+// Prologue, after the wait (the QKV GEMV's raw output is then visible):
+//   ATTN_TALKER  per-head RMSNorm of q and of the new k with the shared [d] weights (QK_NORM_SRC),
+//                rotate_half rope from the cos/sin table at pos (ROPE_SRC), and the KV append
+//                (APPEND_SRC) done by the CTA whose chunk holds pos.
+//   ATTN_RING    interleaved-pair rope (rope_push_src); the CTA whose chunk holds slot pos % ring
+//                writes k, v and the position stamp into the ring.  A slot is legal iff its stamp
+//                is not empty, not after pos, and pos - stamp < window (attn_src).
+//   ATTN_PLAIN   q is taken as given; keys 0..len-1.
+// Each CTA produces, per q head, the chunk's max score m_c, sum l_c = sum_j exp(s_j - m_c) and
+// o_c = sum_j exp(s_j - m_c) v_j.  The last CTA of a (stream, kv head) to finish -- found with an
+// atomic ticket, no waiting -- merges them: out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c,
+// the running-max rescaling of the online softmax (prior art: REL_POS_ATTN on the Parakeet page).
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dec {
+
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
+
+size_t attention_smem_bytes(int d, int group) {
+    (void)group;
+    // K tile, V tile, q [kMaxGroup][d], scores [kMaxGroup][chunk], new k and v [d] each,
+    // stamps [chunk]
+    return sizeof(float) * ((size_t)2 * kAttnChunk * d + (size_t)kMaxGroup * d +
+                            (size_t)kMaxGroup * kAttnChunk + 2 * (size_t)d) +
+           sizeof(uint32_t) * kAttnChunk;
+}
+
+size_t attention_part_bytes(int m, int H, int max_chunks, int d) {
+    return sizeof(float) * (size_t)m * H * max_chunks * d;
+}
+size_t attention_ml_bytes(int m, int H, int max_chunks) {
+    return sizeof(float) * 2 * (size_t)m * H * max_chunks;
+}
+
+// PER consecutive floats from shared memory as one 8- or 16-byte access
+template <int PER>
+__device__ __forceinline__ void load_vec(float* dst, const float* src) {
+    if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        dst[0] = v.x;
+        dst[1] = v.y;
+        dst[2] = v.z;
+        dst[3] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        dst[0] = v.x;
+        dst[1] = v.y;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) {
+    constexpr int CH = kAttnChunk;
+    constexpr int HALF = D / 2;
+    extern __shared__ __align__(128) float smem[];
+    float* Ks = smem;                          // [CH][D]
+    float* Vs = Ks + CH * D;                   // [CH][D]
+    float* qs = Vs + CH * D;                   // [kMaxGroup][D]
+    float* sc = qs + kMaxGroup * D;            // [kMaxGroup][CH]
+    float* knew = sc + kMaxGroup * CH;         // [D]
+    float* vnew = knew + D;                    // [D]
+    uint32_t* stamp = reinterpret_cast<uint32_t*>(vnew + D);  // [CH]
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float s_m[kMaxGroup], s_l[kMaxGroup];
+    __shared__ int s_last;
+
+    const int c = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int mode = p.mode;
+    const int group = p.H / p.G;
+    const float scale = 1.0f / sqrtf((float)D);
+
+    // ---- which keys this CTA owns ---------------------------------------------------------
+    int pos = 0, nch, k0 = c * CH, nk, ncached, newrow = -1;
+    if (mode == ATTN_PLAIN) {
+        const int L = p.len[r];
+        nch = (L + CH - 1) / CH;
+        nk = min(CH, L - k0);
+        ncached = nk;
+    } else if (mode == ATTN_TALKER) {
+        pos = p.len[r];
+        const int L = pos + 1;
+        nch = (L + CH - 1) / CH;
+        nk = min(CH, L - k0);
+        ncached = min(nk, pos - k0);
+        if (pos >= k0 && pos < k0 + CH) newrow = pos - k0;
+    } else {
+        pos = p.len[r];
+        nch = (p.slots + CH - 1) / CH;
+        nk = min(CH, p.slots - k0);
+        ncached = nk;
+        const int slot = pos % p.slots;
+        if (slot >= k0 && slot < k0 + CH) newrow = slot - k0;
+    }
+    const bool bad = (mode != ATTN_PLAIN && (pos < 0 || pos >= p.max_pos ||
+                                             (mode == ATTN_TALKER && pos >= p.slots))) ||
+                     (mode == ATTN_PLAIN && (nch > p.max_chunks || p.len[r] > p.slots ||
+                                             p.len[r] < 1));
+    if (bad || c >= nch) {
+        if (bad && c == 0 && g == 0 && tid == 0) flag_check(p.status, CHECK_BOUNDS);
+        pdl_trigger();
+        pdl_wait();
+        return;
+    }
+
+    // ---- stage the cached rows of the chunk (independent of the previous kernel) ------------
+    const size_t head_base = ((size_t)r * p.G + g) * p.slots;
+    const uint32_t bar_a = smem_u32(&bar);
+    if (tid == 0) {
+        mbar_init(bar_a, 1);
+        const uint32_t bytes = (uint32_t)(ncached > 0 ? ncached : 0) * D * sizeof(float);
+        mbar_arrive_expect_tx(bar_a, 2 * bytes);
+        if (bytes) {
+            bulk_g2s(smem_u32(Ks), p.kc + (head_base + k0) * D, bytes, bar_a);
+            bulk_g2s(smem_u32(Vs), p.vc + (head_base + k0) * D, bytes, bar_a);
+        }
+    }
+    __syncthreads();  // the barrier is initialised before any thread waits on it
+    pdl_trigger();
+    pdl_wait();
+
+    // ---- prologue: q heads of the group (and the new key) -----------------------------------
+    for (int i = warp; i < group; i += kAttnWarps) {
+        const int hq = g * group + i;
+        if (mode == ATTN_PLAIN) {
+            for (int t = lane; t < D; t += 32) qs[i * D + t] = p.qkv[((size_t)r * p.H + hq) * D + t];
+        } else if (mode == ATTN_TALKER) {
+            const float* src = p.qkv + (size_t)r * p.ldqkv + (size_t)hq * D;
+            float v[D / 32];
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+                v[j] = src[lane + 32 * j];
+                ss += v[j] * v[j];
+            }
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss / (float)D + p.eps);
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) v[j] = v[j] * inv * p.qn[lane + 32 * j];
+            const float* cs = p.rope_cos + (size_t)pos * HALF;
+            const float* sn = p.rope_sin + (size_t)pos * HALF;
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+                const int t = lane + 32 * j;
+                const int jj = (j + D / 64) % (D / 32);       // element t +- D/2, same lane
+                const float rot = (t < HALF) ? -v[jj] : v[jj];
+                const int f = t < HALF ? t : t - HALF;
+                qs[i * D + t] = v[j] * cs[f] + rot * sn[f];
+            }
+        } else {
+            const float* src = p.qkv + (size_t)r * p.ldqkv + (size_t)hq * D;
+            const float* cs = p.rope_cos + (size_t)pos * HALF;
+            const float* sn = p.rope_sin + (size_t)pos * HALF;
+            for (int j = lane; j < HALF; j += 32) {
+                const float a = src[2 * j], b = src[2 * j + 1];
+                qs[i * D + 2 * j] = a * cs[j] - b * sn[j];
+                qs[i * D + 2 * j + 1] = a * sn[j] + b * cs[j];
+            }
+        }
+    }
+    if (newrow >= 0 && warp == (group % kAttnWarps)) {
+        // the new key and value of kv head g at position pos
+        if (mode == ATTN_TALKER) {
+            const float* ksrc = p.qkv + (size_t)r * p.ldqkv + (size_t)p.H * D + (size_t)g * D;
+            const float* vsrc = ksrc + (size_t)p.G * D;
+            float v[D / 32];
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+                v[j] = ksrc[lane + 32 * j];
+                ss += v[j] * v[j];
+            }
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss / (float)D + p.eps);
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) v[j] = v[j] * inv * p.kn[lane + 32 * j];
+            const float* cs = p.rope_cos + (size_t)pos * HALF;
+            const float* sn = p.rope_sin + (size_t)pos * HALF;
+#pragma unroll
+            for (int j = 0; j < D / 32; ++j) {
+                const int t = lane + 32 * j;
+                const int jj = (j + D / 64) % (D / 32);
+                const float rot = (t < HALF) ? -v[jj] : v[jj];
+                const int f = t < HALF ? t : t - HALF;
+                knew[t] = v[j] * cs[f] + rot * sn[f];
+                vnew[t] = vsrc[t];
+            }
+        } else {
+            const int D_model = p.H * D;
+            const float* ksrc = p.qkv + (size_t)r * p.ldqkv + D_model + (size_t)g * D;
+            const float* vsrc = ksrc + D_model;
+            const float* cs = p.rope_cos + (size_t)pos * HALF;
+            const float* sn = p.rope_sin + (size_t)pos * HALF;
+            for (int j = lane; j < HALF; j += 32) {
+                const float a = ksrc[2 * j], b = ksrc[2 * j + 1];
+                knew[2 * j] = a * cs[j] - b * sn[j];
+                knew[2 * j + 1] = a * sn[j] + b * cs[j];
+                vnew[2 * j] = vsrc[2 * j];
+                vnew[2 * j + 1] = vsrc[2 * j + 1];
+            }
+        }
+    }
+    if (mode == ATTN_RING)
+        for (int j = tid; j < nk; j += kAttnThreads)
+            stamp[j] = p.pr[(size_t)r * p.slots + k0 + j];
+
+    // ---- wait for the staged rows (bounded) ---------------------------------------------------
+    const bool ok = mbar_wait_bounded(bar_a, 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) flag_check(p.status, CHECK_WAIT_LIMIT);
+        mbar_wait_bounded(bar_a, 0);  // let copies still in flight land before the CTA leaves
+        return;
+    }
+    if (newrow >= 0) {
+        for (int t = tid; t < D; t += kAttnThreads) {
+            Ks[newrow * D + t] = knew[t];
+            Vs[newrow * D + t] = vnew[t];
+        }
+        if (tid == 0 && mode == ATTN_RING) stamp[newrow] = (uint32_t)pos;
+        // append to the cache (after the staged copy has landed: no read/write overlap)
+        float* kd = p.kc + (head_base + k0 + newrow) * D;
+        float* vd = p.vc + (head_base + k0 + newrow) * D;
+        for (int t = tid; t < D; t += kAttnThreads) {
+            kd[t] = knew[t];
+            vd[t] = vnew[t];
+        }
+        if (tid == 0 && mode == ATTN_RING) p.pr[(size_t)r * p.slots + k0 + newrow] = (uint32_t)pos;
+    }
+    __syncthreads();
+
+    // ---- scores: warp per key, lanes split d ---------------------------------------------------
+    constexpr int PER = D / 32;  // dims per lane (contiguous)
+    for (int j = warp; j < nk; j += kAttnWarps) {
+        bool legal = true;
+        if (mode == ATTN_RING) {
+            const uint32_t pj = stamp[j];
+            legal = (pj != 0xFFFFFFFFu) && (pj <= (uint32_t)pos) &&
+                    ((uint32_t)pos - pj < (uint32_t)p.window);
+        }
+        float kv[PER];
+        load_vec<PER>(kv, Ks + j * D + lane * PER);
+        for (int i = 0; i < group; ++i) {
+            float qv[PER];
+            load_vec<PER>(qv, qs + i * D + lane * PER);
+            float a = 0.f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) a += qv[e] * kv[e];
+            a = warp_sum(a);
+            if (lane == 0) sc[i * CH + j] = legal ? a * scale : -CUDART_INF_F;
+        }
+    }
+    __syncthreads();
+
+    // ---- chunk softmax statistics: warp per q head ---------------------------------------------
+    for (int i = warp; i < group; i += kAttnWarps) {
+        float mx = -CUDART_INF_F;
+        for (int j = lane; j < nk; j += 32) mx = fmaxf(mx, sc[i * CH + j]);
+        mx = warp_max(mx);
+        float l = 0.f;
+        for (int j = lane; j < nk; j += 32) {
+            const float e = (mx == -CUDART_INF_F) ? 0.f : expf(sc[i * CH + j] - mx);
+            sc[i * CH + j] = e;
+            l += e;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+            s_m[i] = mx;
+            s_l[i] = l;
+        }
+    }
+    __syncthreads();
+
+    // ---- o_c = sum_j e_j v_j (ascending j), then write the partial ----------------------------
+    for (int o = tid; o < group * D; o += kAttnThreads) {
+        const int i = o / D, t = o - i * D;
+        float acc = 0.f;
+        for (int j = 0; j < nk; ++j) {
+            const float w = sc[i * CH + j];
+            if (w != 0.f) acc += w * Vs[j * D + t];
+        }
+        const int hq = g * group + i;
+        if (nch == 1) {
+            p.out[((size_t)r * p.H + hq) * D + t] = acc / s_l[i];
+        } else {
+            const size_t pi = ((size_t)r * p.H + hq) * p.max_chunks + c;
+            p.part[pi * D + t] = acc;
+            if (t == 0) {
+                p.part_ml[2 * pi] = s_m[i];
+                p.part_ml[2 * pi + 1] = s_l[i];
+            }
+        }
+    }
+    if (nch == 1) return;
+
+    // ---- ticket: the last CTA of (r, g) merges the chunks ---------------------------------------
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&p.tickets[r * p.G + g], 1u);
+        s_last = (prev == (unsigned)(nch - 1));
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    for (int i = warp; i < group; i += kAttnWarps) {
+        const size_t base = ((size_t)r * p.H + g * group + i) * p.max_chunks;
+        float M = -CUDART_INF_F;
+        for (int cc = lane; cc < nch; cc += 32) {
+            const float l = __ldcg(p.part_ml + 2 * (base + cc) + 1);
+            if (l > 0.f) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base + cc)));
+        }
+        M = warp_max(M);
+        float den = 0.f;
+        for (int cc = lane; cc < nch; cc += 32) {
+            const float l = __ldcg(p.part_ml + 2 * (base + cc) + 1);
+            if (l > 0.f) den += expf(__ldcg(p.part_ml + 2 * (base + cc)) - M) * l;
+        }
+        den = warp_sum(den);
+        if (lane == 0) {
+            s_m[i] = M;
+            s_l[i] = den;
+        }
+    }
+    __syncthreads();
+    for (int o = tid; o < group * D; o += kAttnThreads) {
+        const int i = o / D, t = o - i * D;
+        const size_t base = ((size_t)r * p.H + g * group + i) * p.max_chunks;
+        float num = 0.f;
+        for (int cc = 0; cc < nch; ++cc) {
+            const float l = __ldcg(p.part_ml + 2 * (base + cc) + 1);
+            if (l > 0.f)
+                num += expf(__ldcg(p.part_ml + 2 * (base + cc)) - s_m[i]) *
+                       __ldcg(p.part + (base + cc) * D + t);
+        }
+        p.out[((size_t)r * p.H + g * group + i) * D + t] = num / s_l[i];
+    }
+    if (tid == 0) p.tickets[r * p.G + g] = 0u;
+}
+
+template <int D>
+static cudaError_t launch_t(const AttnParams& p, cudaStream_t s, bool pdl) {
+    const size_t smem = attention_smem_bytes(D, p.H / p.G);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.max_chunks, p.G, p.m);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_attention<D>, p);
+}
+
+cudaError_t attention_configure() {
+    cudaError_t e = cudaFuncSetAttribute(k_attention<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)attention_smem_bytes(64, kMaxGroup));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_attention<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attention_smem_bytes(128, kMaxGroup));
+}
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl) {
+    if (p.d == 64) return launch_t<64>(p, s, pdl);
+    if (p.d == 128) return launch_t<128>(p, s, pdl);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace dec

@@ -1,0 +1,138 @@
+// kernels.h -- parameter blocks and launchers of the decode kernels (internal to the library).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dec {
+
+// device check word bits (read back by dec_sync / dec_step_host)
+enum : unsigned {
+    CHECK_WAIT_LIMIT = 1u,   // an mbarrier wait exceeded its iteration bound
+    CHECK_BOUNDS = 2u,       // a position / slot index failed its range check
+};
+
+// ---------------------------------------------------------------------------------------------
+// GEMV: y[r][n] = sum_k W[n][k] * xin[r][k], W row-major [N][K], each weight read once for all
+// rows.  An optional norm prologue builds xin from x; an epilogue consumes the row sums.
+// ---------------------------------------------------------------------------------------------
+enum Prologue : int { PRO_NONE = 0, PRO_RMS = 1, PRO_LN = 2 };
+enum Epilogue : int {
+    EPI_STORE = 0,   // y[r][n] = v
+    EPI_RESID = 1,   // y[r][n] = res[r][n] + (ls ? ls[n] * v : v)   (o-proj / down / MV_LS)
+    EPI_SWIGLU = 2,  // rows interleaved (gate j, up j): y[r][j] = silu(v_2j) * v_2j+1
+    EPI_GELU = 3,    // y[r][n] = 0.5 v (1 + erf(v / sqrt 2))
+};
+
+struct GemvParams {
+    const void* W;
+    int N, K;
+    int m;                 // active rows
+    const float* x;        // [m][ldx]
+    int ldx;
+    int pro;               // Prologue
+    const float* nw;       // norm weight [K]
+    const float* nb;       // LayerNorm bias [K]
+    float eps;
+    int epi;               // Epilogue
+    float* y;              // [m][ldy]
+    int ldy;
+    const float* res;      // residual input [m][ldres] (may alias y)
+    int ldres;
+    const float* ls;       // LayerScale [N] or null
+    float* tap;            // optional copy of y rows [m][ldtap] (EPI_RESID)
+    int ldtap;
+};
+
+// dtype: 0 f32, 1 bf16.  Launches with the programmatic-dependency attribute when pdl.
+// gemv_configure() must have run on the current device first (see configure_kernels).
+constexpr int kGemvMaxSmem = 200 * 1024;
+cudaError_t launch_gemv(const GemvParams& p, int dtype, int num_sms, cudaStream_t s, bool pdl);
+cudaError_t gemv_configure();
+size_t gemv_smem_bytes(int m, int K);
+
+// ---------------------------------------------------------------------------------------------
+// Split-K decode attention with the step's prologue fused in front of it.
+// ---------------------------------------------------------------------------------------------
+enum AttnMode : int {
+    ATTN_PLAIN = 0,   // q given; keys 0..lens[r]-1 of the cache; nothing appended
+    ATTN_TALKER = 1,  // raw qkv: per-head q/k RMSNorm, rotate_half rope, append K/V at pos
+    ATTN_RING = 2,    // raw qkv: interleaved rope, push K/V into slot pos % ring, stamp it;
+                      // keys legal by stamp and window
+};
+
+constexpr int kAttnChunk = 64;   // keys per CTA
+constexpr int kMaxGroup = 8;     // q heads per kv head handled by one CTA
+
+struct AttnParams {
+    int mode;
+    int m;                 // rows (streams)
+    int H, G, d;           // q heads, kv heads, head_dim
+    int slots;             // cache rows per (stream, kv head): capacity or ring
+    int window;            // ring: attention window
+    const float* qkv;      // TALKER/RING: raw [m][ldqkv] = [q | k | v]; PLAIN: q [m][H][d]
+    int ldqkv;
+    float* kc;             // K cache [m][G][slots][d] (this layer)
+    float* vc;             // V cache
+    uint32_t* pr;          // RING: position stamps [m][slots]
+    const int32_t* len;    // TALKER/RING: [m] current lengths = positions; PLAIN: keys
+    const float* qn;       // TALKER: q norm weight [d]
+    const float* kn;       // TALKER: k norm weight [d]
+    float eps;
+    const float* rope_cos; // [max_pos][d/2]
+    const float* rope_sin;
+    int max_pos;
+    float* part;           // [m][H][max_chunks][d] partial outputs
+    float* part_ml;        // [m][H][max_chunks][2] partial (max, sum)
+    unsigned* tickets;     // [m][G] merge tickets, zero between calls
+    int max_chunks;
+    float* out;            // [m][H*d]
+    unsigned* status;
+};
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl);
+cudaError_t attention_configure();
+size_t attention_smem_bytes(int d, int group);
+// scratch sizes (bytes) for the partials and tickets
+size_t attention_part_bytes(int m, int H, int max_chunks, int d);
+size_t attention_ml_bytes(int m, int H, int max_chunks);
+
+// ---------------------------------------------------------------------------------------------
+// Small kernels: final norm / copy-out + length advance, prefill copy-in, stream reset.
+// ---------------------------------------------------------------------------------------------
+struct FinalParams {
+    int m, h;
+    const float* x;        // residual stream [m][h]
+    const float* w;        // talker final norm [h]; null = copy (codec)
+    float eps;
+    float* out;            // [m][h]
+    int32_t* len;          // [m]: incremented
+};
+cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
+
+struct PrefillParams {
+    int layers, n, G, d, slots, streams, stream;
+    const float* k_src;    // [layers][n][G][d]
+    const float* v_src;
+    float* kc;             // [layers][streams][G][slots][d]
+    float* vc;
+    uint32_t* pr;          // codec: [layers][streams][slots] or null
+    int32_t* len;          // [streams]
+};
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t s);
+
+struct ResetParams {
+    int layers, streams, stream, slots;
+    uint32_t* pr;          // codec stamps or null
+    int32_t* len;
+};
+cudaError_t launch_reset_stamps(const ResetParams& p, cudaStream_t s);
+// len[stream] = value (the value travels as a kernel argument, so the host may reuse it at once)
+cudaError_t launch_set_len(int32_t* len, int stream, int value, cudaStream_t s);
+
+// Set the kernels' shared-memory limits on the current device (once per device; safe to call
+// from several threads).  Must run before a kernel is launched or captured on that device.
+cudaError_t configure_kernels();
+
+}  // namespace dec
