@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=W.TALKER_H2048_L28.name,
                    choices=sorted(W.WORKLOADS))
+    p.add_argument("--layers", type=int, default=0,
+                   help="keep only the first N layers (small cases for profiler captures)")
     p.add_argument("--kernel-rounds", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -245,6 +247,9 @@ def run_ours(args):
     if pg:
         pg.barrier()
     w = W.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, layers=min(args.layers, w.layers))
     talker = w.kind == "talker"
     syn = W.generate(w)
     if not talker:
@@ -317,6 +322,9 @@ def run_ours(args):
     step_gbs = nb / (ms_step * 1e-3) / 1e9
 
     # ---- dominant kernel on its own: one launch per layer, CUDA events around each ----------
+    if talker:
+        for s in range(m):
+            dec.truncate(s, base[s])
     stage, kname, kbytes = dominant_kernel(w, m)
     durs = []
     for _ in range(args.kernel_rounds):

@@ -61,6 +61,29 @@ __device__ __forceinline__ void load_vec(float* dst, const float* src) {
     }
 }
 
+// v[0..7] per lane -> lane l returns the warp-wide sum of v[(l >> 2) & 7]
+__device__ __forceinline__ float butterfly8_attn(const float v[8], int lane) {
+    const bool hi16 = lane & 16, hi8 = lane & 8, hi4 = lane & 4;
+    float a[4], b[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = hi16 ? v[i] : v[i + 4];
+        const float keep = hi16 ? v[i + 4] : v[i];
+        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = hi8 ? a[i] : a[i + 2];
+        const float keep = hi8 ? a[i + 2] : a[i];
+        b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = hi4 ? b[0] : b[1];
+    float c = (hi4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    return c;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) {
     constexpr int CH = kAttnChunk;
@@ -241,25 +264,40 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) 
     }
     __syncthreads();
 
-    // ---- scores: warp per key, lanes split d ---------------------------------------------------
+    // ---- scores: a warp takes 8 keys at a time, lanes split d, one butterfly per head ------------
     constexpr int PER = D / 32;  // dims per lane (contiguous)
-    for (int j = warp; j < nk; j += kAttnWarps) {
-        bool legal = true;
-        if (mode == ATTN_RING) {
-            const uint32_t pj = stamp[j];
-            legal = (pj != 0xFFFFFFFFu) && (pj <= (uint32_t)pos) &&
-                    ((uint32_t)pos - pj < (uint32_t)p.window);
+    for (int j0 = warp * 8; j0 < nk; j0 += kAttnWarps * 8) {
+        float kv[8][PER];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (j0 + u < nk)
+                load_vec<PER>(kv[u], Ks + (j0 + u) * D + lane * PER);
+            else
+#pragma unroll
+                for (int e = 0; e < PER; ++e) kv[u][e] = 0.f;
         }
-        float kv[PER];
-        load_vec<PER>(kv, Ks + j * D + lane * PER);
         for (int i = 0; i < group; ++i) {
             float qv[PER];
             load_vec<PER>(qv, qs + i * D + lane * PER);
-            float a = 0.f;
+            float part[8];
 #pragma unroll
-            for (int e = 0; e < PER; ++e) a += qv[e] * kv[e];
-            a = warp_sum(a);
-            if (lane == 0) sc[i * CH + j] = legal ? a * scale : -CUDART_INF_F;
+            for (int u = 0; u < 8; ++u) {
+                float a = 0.f;
+#pragma unroll
+                for (int e = 0; e < PER; ++e) a += qv[e] * kv[u][e];
+                part[u] = a;
+            }
+            const float sum = butterfly8_attn(part, lane);   // lanes 4u..4u+3 hold key j0 + u
+            const int u = (lane >> 2) & 7;
+            if ((lane & 3) == 0 && j0 + u < nk) {
+                bool legal = true;
+                if (mode == ATTN_RING) {
+                    const uint32_t pj = stamp[j0 + u];
+                    legal = (pj != 0xFFFFFFFFu) && (pj <= (uint32_t)pos) &&
+                            ((uint32_t)pos - pj < (uint32_t)p.window);
+                }
+                sc[i * CH + j0 + u] = legal ? sum * scale : -CUDART_INF_F;
+            }
         }
     }
     __syncthreads();
@@ -286,11 +324,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) 
     // ---- o_c = sum_j e_j v_j (ascending j), then write the partial ----------------------------
     for (int o = tid; o < group * D; o += kAttnThreads) {
         const int i = o / D, t = o - i * D;
+        // masked keys weigh exactly 0 and their V rows hold finite values (zeroed at creation)
         float acc = 0.f;
-        for (int j = 0; j < nk; ++j) {
-            const float w = sc[i * CH + j];
-            if (w != 0.f) acc += w * Vs[j * D + t];
-        }
+        const float* w = sc + i * CH;
+#pragma unroll 8
+        for (int j = 0; j < nk; ++j) acc += w[j] * Vs[j * D + t];
         const int hq = g * group + i;
         if (nch == 1) {
             p.out[((size_t)r * p.H + hq) * D + t] = acc / s_l[i];
@@ -316,37 +354,81 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) 
     if (!s_last) return;
     __threadfence();
 
+    // Stage every chunk's (m, l) of the group's heads in shared memory with independent loads
+    // (the K/V tiles are no longer needed), then the per-head max M, denominator and chunk
+    // weights w_c = exp(m_c - M); chunks without a legal key (l == 0) weigh 0.
+    float* wsc = Ks;                               // [group][nch] chunk weights
+    float* buf = Ks + kMaxGroup * ((p.max_chunks + 3) & ~3);  // partial outputs, batched
+    for (int idx = tid; idx < group * nch; idx += kAttnThreads) {
+        const int i = idx / nch, cc = idx - i * nch;
+        const size_t pi = ((size_t)r * p.H + g * group + i) * p.max_chunks + cc;
+        const float mc = __ldcg(p.part_ml + 2 * pi), lc = __ldcg(p.part_ml + 2 * pi + 1);
+        wsc[i * nch + cc] = lc > 0.f ? mc : -CUDART_INF_F;
+        buf[idx] = lc;
+    }
+    __syncthreads();
     for (int i = warp; i < group; i += kAttnWarps) {
-        const size_t base = ((size_t)r * p.H + g * group + i) * p.max_chunks;
         float M = -CUDART_INF_F;
-        for (int cc = lane; cc < nch; cc += 32) {
-            const float l = __ldcg(p.part_ml + 2 * (base + cc) + 1);
-            if (l > 0.f) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base + cc)));
-        }
+        for (int cc = lane; cc < nch; cc += 32) M = fmaxf(M, wsc[i * nch + cc]);
         M = warp_max(M);
         float den = 0.f;
         for (int cc = lane; cc < nch; cc += 32) {
-            const float l = __ldcg(p.part_ml + 2 * (base + cc) + 1);
-            if (l > 0.f) den += expf(__ldcg(p.part_ml + 2 * (base + cc)) - M) * l;
+            const float mc = wsc[i * nch + cc];
+            const float wc = (mc == -CUDART_INF_F) ? 0.f : expf(mc - M);
+            wsc[i * nch + cc] = wc;
+            den += wc * buf[i * nch + cc];
         }
         den = warp_sum(den);
-        if (lane == 0) {
-            s_m[i] = M;
-            s_l[i] = den;
-        }
+        if (lane == 0) s_l[i] = den;
     }
     __syncthreads();
-    for (int o = tid; o < group * D; o += kAttnThreads) {
-        const int i = o / D, t = o - i * D;
-        const size_t base = ((size_t)r * p.H + g * group + i) * p.max_chunks;
-        float num = 0.f;
-        for (int cc = 0; cc < nch; ++cc) {
-            const float l = __ldcg(p.part_ml + 2 * (base + cc) + 1);
-            if (l > 0.f)
-                num += expf(__ldcg(p.part_ml + 2 * (base + cc)) - s_m[i]) *
-                       __ldcg(p.part + (base + cc) * D + t);
+    // out = sum_c w_c o_c / den, the partial rows fetched in batches of whole chunks
+    const int per_batch = (int)((2 * CH * D - kMaxGroup * ((p.max_chunks + 3) & ~3)) / (group * D));
+    float num[(kMaxGroup * D + kAttnThreads - 1) / kAttnThreads];
+#pragma unroll
+    for (int q = 0; q < (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads; ++q) num[q] = 0.f;
+    for (int c0 = 0; c0 < nch; c0 += per_batch) {
+        const int nb = min(per_batch, nch - c0);
+        const int total = nb * group * D;
+        constexpr int UNR = 16;  // independent loads in flight per thread
+        for (int base = 0; base < total; base += kAttnThreads * UNR) {
+            float tmp[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int idx = base + u * kAttnThreads + tid;
+                tmp[u] = 0.f;
+                if (idx < total) {
+                    const int cc = idx / (group * D), rem = idx - cc * group * D;
+                    const int i = rem / D, t = rem - i * D;
+                    const size_t pi = ((size_t)r * p.H + g * group + i) * p.max_chunks + c0 + cc;
+                    tmp[u] = __ldcg(p.part + pi * D + t);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int idx = base + u * kAttnThreads + tid;
+                if (idx < total) buf[idx] = tmp[u];
+            }
         }
-        p.out[((size_t)r * p.H + g * group + i) * D + t] = num / s_l[i];
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads; ++q) {
+            const int o = tid + q * kAttnThreads;
+            if (o < group * D) {
+                const int i = o / D;
+                for (int cc = 0; cc < nb; ++cc)
+                    num[q] += wsc[i * nch + c0 + cc] * buf[cc * group * D + o];
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int q = 0; q < (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads; ++q) {
+        const int o = tid + q * kAttnThreads;
+        if (o < group * D) {
+            const int i = o / D, t = o - i * D;
+            p.out[((size_t)r * p.H + g * group + i) * D + t] = num[q] / s_l[i];
+        }
     }
     if (tid == 0) p.tickets[r * p.G + g] = 0u;
 }

@@ -160,6 +160,8 @@ dec_status validate_config(const dec_config* c) {
         return fail(nullptr, DEC_E_ARG, "norm_eps must be finite and >= 0");
     if (!(c->rope_theta > 0.0) || !std::isfinite(c->rope_theta))
         return fail(nullptr, DEC_E_ARG, "rope_theta must be finite and > 0");
+    if ((c->kind == DEC_QWEN3_TALKER ? c->max_pos : c->ring) > kMaxSlots)
+        return fail(nullptr, DEC_E_UNSUPPORTED, "KV capacity above %d positions", kMaxSlots);
     if (c->kind == DEC_CODEC_WINDOWED) {
         if (c->kv_heads != c->q_heads)
             return fail(nullptr, DEC_E_ARG, "codec layers are multi-head: kv_heads == q_heads");
@@ -212,6 +214,7 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
     GemvParams g = {};
     g.m = m;
     g.eps = c.norm_eps;
+    g.status = ctx->status;
     switch (stage) {
         case 0:  // norm + q/k/v
             g.W = talker ? W.qkv : W.in_proj;
@@ -817,6 +820,7 @@ dec_status dec_attention(int m, int q_heads, int kv_heads, int head_dim, int cap
     if (!q || !k || !v || !lens || !out || !workspace) return fail(nullptr, DEC_E_ARG, "NULL pointer");
     if (m < 1 || m > 64 || capacity < 1 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads)
         return fail(nullptr, DEC_E_ARG, "bad m, capacity or head counts");
+    if (capacity > kMaxSlots) return fail(nullptr, DEC_E_UNSUPPORTED, "capacity above %d", kMaxSlots);
     if (head_dim != 64 && head_dim != 128) return fail(nullptr, DEC_E_UNSUPPORTED, "head_dim 64 or 128");
     if (q_heads / kv_heads > kMaxGroup) return fail(nullptr, DEC_E_UNSUPPORTED, "GQA group above 8");
     if (!aligned16(k) || !aligned16(v) || !aligned16(workspace))

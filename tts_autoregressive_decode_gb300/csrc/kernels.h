@@ -43,6 +43,12 @@ struct GemvParams {
     const float* ls;       // LayerScale [N] or null
     float* tap;            // optional copy of y rows [m][ldtap] (EPI_RESID)
     int ldtap;
+    unsigned* status;      // device check word (bounded waits), may be null
+    // filled by launch_gemv for the bulk-copy pipeline
+    int rb;                // rows per stage
+    int nstages;           // stages in the ring
+    int unit;              // rows per partition unit (2 for SwiGLU pairs)
+    int stage_stride;      // bytes between ring stages
 };
 
 // dtype: 0 f32, 1 bf16.  Launches with the programmatic-dependency attribute when pdl.
@@ -64,6 +70,7 @@ enum AttnMode : int {
 
 constexpr int kAttnChunk = 64;   // keys per CTA
 constexpr int kMaxGroup = 8;     // q heads per kv head handled by one CTA
+constexpr int kMaxSlots = 32768; // cache rows per (stream, kv head): bounds the merge's staging
 
 struct AttnParams {
     int mode;
