@@ -234,6 +234,26 @@ dec_status dec_attention(int m, int q_heads, int kv_heads, int head_dim, int cap
                          const float* q, const float* k, const float* v, const int32_t* lens,
                          float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* dec_attention without any allocation (no counterpart on the pages: a service of this library).
+ * Some callers cannot allocate device memory: code on a real-time audio thread, where
+ * cudaMalloc/cudaFree may synchronize the device and take unbounded time, and code inside a host
+ * application whose own allocator owns the device-memory budget.  This entry computes exactly
+ * what dec_attention computes, with the same arguments minus the workspace: its scratch is a
+ * static device array of 4 MiB that the library holds on every GPU it is loaded on until the
+ * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   Limit: the scratch dec_attention_workspace_bytes(m, q_heads, kv_heads, head_dim, capacity)
+ *   would report must fit in 4 MiB (e.g. m = 1, 16 q heads, d = 128: capacity up to 32768);
+ *   larger requests return DEC_E_UNSUPPORTED (text in dec_last_error(NULL)).
+ *   The first call on a device looks up the array's device address; make that first call
+ *   outside any stream capture.
+ *   Every call on a device shares the one array: calls that overlap on the GPU (other streams,
+ *   other host threads) race and corrupt each other's results.  Each call clears the words that
+ *   must start at zero before its kernel runs.
+ * Asynchronous on `stream`; same layouts, limits and errors as dec_attention otherwise. */
+dec_status dec_attention_noalloc(int m, int q_heads, int kv_heads, int head_dim, int capacity,
+                                 const float* q, const float* k, const float* v,
+                                 const int32_t* lens, float* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,8 @@ DEC_FLAG_TAPS, DEC_FLAG_NO_GRAPH = 1, 2
 EXPORTS = ("dec_create", "dec_destroy", "dec_last_error", "dec_set_stream", "dec_prefill_kv",
            "dec_step", "dec_step_host", "dec_reset", "dec_sync", "dec_get_len", "dec_read_kv",
            "dec_read_tap", "dec_kernels_per_step", "dec_truncate", "dec_launch_stage",
-           "dec_gemv", "dec_attention_workspace_bytes", "dec_attention")
+           "dec_gemv", "dec_attention_workspace_bytes", "dec_attention",
+           "dec_attention_noalloc")
 
 
 class DecConfig(C.Structure):
@@ -91,8 +92,10 @@ def load() -> C.CDLL:
         L.dec_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.dec_attention_workspace_bytes.restype = sz
         L.dec_attention.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dec_attention_noalloc.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         for f in ("dec_set_stream", "dec_prefill_kv", "dec_step", "dec_step_host", "dec_reset",
                   "dec_sync", "dec_read_kv", "dec_read_tap", "dec_gemv", "dec_attention",
+                  "dec_attention_noalloc",
                   "dec_truncate", "dec_launch_stage"):
             getattr(L, f).restype = i32
         L.dec_get_len.restype = i32

@@ -396,6 +396,11 @@ dec_status read_status(dec_ctx* ctx) {
 
 }  // namespace
 
+namespace dec {
+// record a failure of a context-free entry point (read back with dec_last_error(NULL))
+dec_status stateless_fail(dec_status st, const char* msg) { return fail(nullptr, st, "%s", msg); }
+}  // namespace dec
+
 // =============================================================================================
 // exported entry points
 // =============================================================================================
