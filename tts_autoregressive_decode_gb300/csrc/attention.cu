@@ -45,22 +45,6 @@ size_t attention_ml_bytes(int m, int H, int max_chunks) {
     return sizeof(float) * 2 * (size_t)m * H * max_chunks;
 }
 
-// PER consecutive floats from shared memory as one 8- or 16-byte access
-template <int PER>
-__device__ __forceinline__ void load_vec(float* dst, const float* src) {
-    if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        dst[0] = v.x;
-        dst[1] = v.y;
-        dst[2] = v.z;
-        dst[3] = v.w;
-    } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        dst[0] = v.x;
-        dst[1] = v.y;
-    }
-}
-
 // v[0..7] per lane -> lane l returns the warp-wide sum of v[(l >> 2) & 7]
 __device__ __forceinline__ float butterfly8_attn(const float v[8], int lane) {
     const bool hi16 = lane & 16, hi8 = lane & 8, hi4 = lane & 4;
@@ -341,7 +325,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) 
             }
         }
     }
-    if (nch == 1) return;
+    // with no ticket array the partials are merged by the separate merge kernel
+    if (nch == 1 || !p.tickets) return;
 
     // ---- ticket: the last CTA of (r, g) merges the chunks ---------------------------------------
     __threadfence();
@@ -447,6 +432,76 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t s, bool pdl) {
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, k_attention<D>, p);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Merge of the chunk partials, one CTA per (q head, stream), d threads:
+// out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c over the chunks with a legal key (l_c > 0).
+// Launched after k_attention (programmatic dependent); the chunking is k_attention's.
+// ---------------------------------------------------------------------------------------------
+constexpr int kMergeBatch = 64;  // partial rows in flight per thread
+
+template <int D>
+__global__ void __launch_bounds__(D) k_attn_merge(const AttnParams p) {
+    constexpr int CH = kAttnChunk;
+    __shared__ float sm[kMaxSlots / kAttnChunk], sw[kMaxSlots / kAttnChunk];
+    const int hq = blockIdx.x, r = blockIdx.y, t = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    int L;
+    if (p.mode == ATTN_PLAIN) L = p.len[r];
+    else L = (p.mode == ATTN_TALKER) ? p.len[r] + 1 : p.slots;
+    const int nch = (L + CH - 1) / CH;
+    if (L < 1 || nch <= 1 || nch > p.max_chunks) return;  // one chunk: k_attention wrote out
+    const size_t base = ((size_t)r * p.H + hq) * p.max_chunks;
+    for (int c = t; c < nch; c += D) {
+        const float l = __ldcg(p.part_ml + 2 * (base + c) + 1);
+        sm[c] = l > 0.f ? __ldcg(p.part_ml + 2 * (base + c)) : -CUDART_INF_F;
+        sw[c] = l;
+    }
+    __syncthreads();
+    float M = -CUDART_INF_F;
+    for (int c = 0; c < nch; ++c) M = fmaxf(M, sm[c]);
+    __syncthreads();
+    for (int c = t; c < nch; c += D) {  // weight of chunk c, and its share of the denominator
+        const float w = sm[c] == -CUDART_INF_F ? 0.f : expf(sm[c] - M);
+        sm[c] = w;
+        sw[c] = w * sw[c];
+    }
+    __syncthreads();
+    float den = 0.f, num = 0.f;
+    for (int c = 0; c < nch; ++c) den += sw[c];
+    for (int c0 = 0; c0 < nch; c0 += kMergeBatch) {
+        float v[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u)
+            v[u] = c0 + u < nch ? __ldcg(p.part + (base + c0 + u) * D + t) : 0.f;
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u)
+            if (c0 + u < nch) num += sm[c0 + u] * v[u];
+    }
+    p.out[((size_t)r * p.H + hq) * D + t] = num / den;
+}
+
+template <int D>
+static cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.H, p.m);
+    cfg.blockDim = dim3(D);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_attn_merge<D>, p);
+}
+
+cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl) {
+    if (p.max_chunks > kMaxSlots / kAttnChunk) return cudaErrorInvalidValue;
+    if (p.d == 64) return launch_merge_t<64>(p, s, pdl);
+    if (p.d == 128) return launch_merge_t<128>(p, s, pdl);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t attention_configure() {

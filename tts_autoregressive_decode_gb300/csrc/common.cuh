@@ -83,9 +83,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-// Hint: pull [src, src + bytes) into L2 (bytes a multiple of 16, src 16-byte aligned).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+// ---- L2 cache policy -----------------------------------------------------------------------
+// evict_first: data streamed once (weights), so it does not push out data that is reused
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // ---- loads ---------------------------------------------------------------------------------
@@ -95,6 +98,15 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+    return v;
+}
+
+// ... with an L2 policy (weights: evict_first)
+__device__ __forceinline__ uint4 ld_stream16(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
     return v;
 }
 
@@ -116,6 +128,22 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 // a 32-bit word holding two bf16 values (low half first) -> the two exact f32 values
 __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// PER (2 or 4) consecutive floats from shared memory as one 8- or 16-byte access
+template <int PER>
+__device__ __forceinline__ void load_vec(float* dst, const float* src) {
+    if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        dst[0] = v.x;
+        dst[1] = v.y;
+        dst[2] = v.z;
+        dst[3] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        dst[0] = v.x;
+        dst[1] = v.y;
+    }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -1,11 +1,12 @@
 // dec_api.cu -- the C ABI (include/dec.h): context state, the step plan, CUDA-graph replay.
 //
-// Plan of one step of m rows (per layer, five kernels chained with programmatic dependent
+// Plan of one step of m rows (per layer, six kernels chained with programmatic dependent
 // launch, then one final kernel):
-//   talker: [RMSNorm + QKV GEMV] -> [qk-norm + rope + append + split-K GQA attention + merge]
-//           -> [o-proj GEMV + residual] -> [RMSNorm + gate/up GEMV + SwiGLU]
-//           -> [down GEMV + residual]; final RMSNorm (+ length advance)
-//   codec:  [LayerNorm + qkv GEMV] -> [rope + ring push + windowed attention + merge]
+//   talker: [RMSNorm + QKV GEMV] -> [qk-norm + rope + append + split-K GQA attention chunks]
+//           -> [merge of the chunks] -> [o-proj GEMV + residual]
+//           -> [RMSNorm + gate/up GEMV + SwiGLU] -> [down GEMV + residual];
+//           final RMSNorm (+ length advance)
+//   codec:  [LayerNorm + qkv GEMV] -> [rope + ring push + windowed attention chunks] -> [merge]
 //           -> [out-proj GEMV + LayerScale residual] -> [LayerNorm + lin1 GEMV + GELU]
 //           -> [lin2 GEMV + LayerScale residual]; copy-out (+ length advance)
 // The sequence is the talker's build_step_plan and Mimi's transformer_shaped with the
@@ -89,7 +90,7 @@ struct dec_ctx {
     int S = 0;              // streams
     int slots = 0;          // KV rows per (layer, stream, kv head)
     int qkv_rows = 0;       // rows of the fused q/k/v matrix
-    int max_chunks = 0;
+    int max_chunks = 0;     // attention chunks per (stream, kv head)
     char* arena = nullptr;  // weights
     std::vector<LayerW> L;
     const float* final_norm = nullptr;
@@ -98,8 +99,7 @@ struct dec_ctx {
     uint32_t* pr = nullptr;
     float *rope_cos = nullptr, *rope_sin = nullptr;
     float *xres = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr;
-    float *part = nullptr, *part_ml = nullptr;
-    unsigned* tickets = nullptr;
+    float *part = nullptr, *part_ml = nullptr;  // attention chunk partials
     int32_t* len_dev = nullptr;
     unsigned* status = nullptr;
     float* taps = nullptr;
@@ -160,8 +160,6 @@ dec_status validate_config(const dec_config* c) {
         return fail(nullptr, DEC_E_ARG, "norm_eps must be finite and >= 0");
     if (!(c->rope_theta > 0.0) || !std::isfinite(c->rope_theta))
         return fail(nullptr, DEC_E_ARG, "rope_theta must be finite and > 0");
-    if ((c->kind == DEC_QWEN3_TALKER ? c->max_pos : c->ring) > kMaxSlots)
-        return fail(nullptr, DEC_E_UNSUPPORTED, "KV capacity above %d positions", kMaxSlots);
     if (c->kind == DEC_CODEC_WINDOWED) {
         if (c->kv_heads != c->q_heads)
             return fail(nullptr, DEC_E_ARG, "codec layers are multi-head: kv_heads == q_heads");
@@ -170,6 +168,8 @@ dec_status validate_config(const dec_config* c) {
         if (c->ring < 1 || c->window < 1 || c->window > c->ring)
             return fail(nullptr, DEC_E_ARG, "codec: need 1 <= window <= ring");
     }
+    if ((c->kind == DEC_QWEN3_TALKER ? c->max_pos : c->ring) > kMaxSlots)
+        return fail(nullptr, DEC_E_UNSUPPORTED, "KV capacity above %d positions", kMaxSlots);
     const int widest = std::max(std::max(c->hidden, c->inter), c->q_heads * c->head_dim);
     if (gemv_smem_bytes(c->max_streams, widest) > 200 * 1024)
         return fail(nullptr, DEC_E_UNSUPPORTED,
@@ -252,11 +252,13 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
             a.max_pos = c.max_pos;
             a.part = ctx->part;
             a.part_ml = ctx->part_ml;
-            a.tickets = ctx->tickets;
+            a.tickets = nullptr;  // partials are merged by the merge kernel below
             a.max_chunks = ctx->max_chunks;
             a.out = ctx->attn;
             a.status = ctx->status;
-            return launch_attention(a, s, pdl);
+            cudaError_t e = launch_attention(a, s, pdl);
+            if (e != cudaSuccess) return e;
+            return launch_attention_merge(a, s, true);
         }
         case 2:  // o-proj + residual (codec: LayerScale)
             g.W = talker ? W.o : W.out_proj;
@@ -438,7 +440,6 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->S = c.max_streams;
     ctx->slots = talker ? c.max_pos : c.ring;
     ctx->qkv_rows = talker ? (H + 2 * G) * d : 3 * h;
-    ctx->max_chunks = (ctx->slots + kAttnChunk - 1) / kAttnChunk;
     ctx->num_sms = device_sm_count();
     ctx->len_host.assign(ctx->S, 0);
     auto bail = [&](dec_status s) {
@@ -452,6 +453,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     }
     cudaError_t e = configure_kernels();
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "kernel attributes"));
+    ctx->max_chunks = (ctx->slots + kAttnChunk - 1) / kAttnChunk;
     e = cudaStreamCreateWithFlags(&ctx->cap_stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "capture stream"));
     if ((e = cudaMallocHost(&ctx->status_host, sizeof(unsigned))) != cudaSuccess)
@@ -564,7 +566,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     const size_t o_att = take((size_t)S * qw * 4), o_act = take((size_t)S * I * 4);
     const size_t o_part = take(attention_part_bytes(S, H, ctx->max_chunks, d));
     const size_t o_ml = take(attention_ml_bytes(S, H, ctx->max_chunks));
-    const size_t o_tk = take((size_t)S * G * 4), o_len = take((size_t)S * 4), o_st = take(4);
+    const size_t o_len = take((size_t)S * 4), o_st = take(4);
     const size_t o_taps = (c.flags & DEC_FLAG_TAPS) ? take((size_t)c.layers * S * h * 4) : 0;
     const size_t o_in = take((size_t)S * h * 4), o_out = take((size_t)S * h * 4);
     if ((e = cudaMalloc(&ctx->state, tot)) != cudaSuccess) return bail(cuda_fail(ctx, e, "state"));
@@ -580,13 +582,12 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->act = reinterpret_cast<float*>(b + o_act);
     ctx->part = reinterpret_cast<float*>(b + o_part);
     ctx->part_ml = reinterpret_cast<float*>(b + o_ml);
-    ctx->tickets = reinterpret_cast<unsigned*>(b + o_tk);
     ctx->len_dev = reinterpret_cast<int32_t*>(b + o_len);
     ctx->status = reinterpret_cast<unsigned*>(b + o_st);
     ctx->taps = (c.flags & DEC_FLAG_TAPS) ? reinterpret_cast<float*>(b + o_taps) : nullptr;
     ctx->io_in = reinterpret_cast<float*>(b + o_in);
     ctx->io_out = reinterpret_cast<float*>(b + o_out);
-    // everything zero (K/V, scratch, tickets, lengths, status), then the stamps to empty
+    // everything zero (K/V, scratch, lengths, status), then the stamps to empty
     if ((e = cudaMemsetAsync(ctx->state, 0, tot, s)) != cudaSuccess)
         return bail(cuda_fail(ctx, e, "state clear"));
     if (!talker && (e = cudaMemsetAsync(ctx->pr, 0xFF, (size_t)c.layers * S * ctx->slots * 4, s)) !=
@@ -753,7 +754,7 @@ dec_status dec_read_tap(dec_ctx* ctx, int layer, int m, float* dst_host) {
 
 int dec_kernels_per_step(const dec_ctx* ctx, int m) {
     if (!ctx || m < 1 || m > ctx->S) return -1;
-    return 5 * ctx->cfg.layers + 1;
+    return 6 * ctx->cfg.layers + 1;
 }
 
 dec_status dec_truncate(dec_ctx* ctx, int stream, int new_len) {

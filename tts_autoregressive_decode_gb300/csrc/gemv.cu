@@ -322,6 +322,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) k_gemv_rows(const GemvParams 
         gj[j] = (j * kRowsWarps + warp) * 32 + lane;
         ok[j] = gj[j] < G;
     }
+    const uint64_t pol = l2_evict_first();
     uint4 wa[RB][NJ], wb[RB][NJ];
     auto load = [&](uint4 (&w)[RB][NJ], int b0) {
 #pragma unroll
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kRowsThreads, 2) k_gemv_rows(const GemvParams 
 #pragma unroll
             for (int j = 0; j < NJ; ++j)
                 w[r][j] = (b0 + r < nrows && ok[j])
-                              ? ld_stream16(Wb + (size_t)(b0 + r) * row_bytes + (size_t)gj[j] * 16)
+                              ? ld_stream16(Wb + (size_t)(b0 + r) * row_bytes + (size_t)gj[j] * 16, pol)
                               : make_uint4(0u, 0u, 0u, 0u);
     };
 

@@ -92,7 +92,7 @@ struct AttnParams {
     int max_pos;
     float* part;           // [m][H][max_chunks][d] partial outputs
     float* part_ml;        // [m][H][max_chunks][2] partial (max, sum)
-    unsigned* tickets;     // [m][G] merge tickets, zero between calls
+    unsigned* tickets;     // [m][G] merge tickets, zero between calls; null: no in-kernel merge
     int max_chunks;
     float* out;            // [m][H*d]
     unsigned* status;
@@ -100,6 +100,8 @@ struct AttnParams {
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl);
 cudaError_t attention_configure();
+// Merge of k_attention's chunk partials (launch after k_attention with tickets == nullptr).
+cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl);
 size_t attention_smem_bytes(int d, int group);
 // scratch sizes (bytes) for the partials and tickets
 size_t attention_part_bytes(int m, int H, int max_chunks, int d);
