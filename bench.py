@@ -42,7 +42,12 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch of the dominant kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), with the hash of the kernel source it was taken on.  A changed kernel
 # reports null until it is captured again.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # gate/up GEMV (k_gemv_rows<bf16, m1, NJ1>, N = 12288, K = 2048): one launch captured with
+    # ncu --set full on the 2-layer case of the same shapes (profiles/k_gemv_rows_gateup_*.md);
+    # a launch does the same work at any layer count
+    W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_381_312, "source_sha": "3bdd5a5d53c5516a"},
+}
 
 
 def parse():
@@ -56,6 +61,8 @@ def parse():
     p.add_argument("--layers", type=int, default=0,
                    help="keep only the first N layers (small cases for profiler captures)")
     p.add_argument("--kernel-rounds", type=int, default=20)
+    p.add_argument("--plan", choices=["kernels", "persistent"], default="kernels",
+                   help="step plan: the chain of kernels (default) or the persistent kernel")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -100,8 +107,15 @@ def dominant_kernel(w: W.Workload, m: int):
 
 
 def kernel_source_sha() -> str:
-    src = os.path.join(ROOT, "tts_autoregressive_decode_gb300", "csrc", "gemv.cu")
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    """Hash of every kernel source file: a stored ncu traffic figure is only reported for the
+    sources it was measured on."""
+    d = os.path.join(ROOT, "tts_autoregressive_decode_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -255,7 +269,8 @@ def run_ours(args):
     if not talker:
         # the ring keeps positions growing: size the RoPE table for warm-up + timed + e2e steps
         syn.max_pos = max(syn.max_pos, 2 * (args.warmup + args.steps) + 2 * w.steps + 8)
-    dec = Decoder.from_synthetic(syn)
+    from tts_autoregressive_decode_gb300 import _lib
+    dec = Decoder.from_synthetic(syn, flags=_lib.DEC_FLAG_PERSISTENT if args.plan == "persistent" else 0)
     m, h = w.streams, w.hidden
     base = list(syn.lengths)
     X = torch.from_numpy(syn.inputs).cuda()                  # [steps][m][h], resident in HBM
@@ -321,33 +336,41 @@ def run_ours(args):
     peak, peak_src = peaks()
     step_gbs = nb / (ms_step * 1e-3) / 1e9
 
-    # ---- dominant kernel on its own: one launch per layer captured in a CUDA graph (no host
-    # launch cost in the timing), replayed between CUDA events on the replay stream ------------
-    if talker:
-        for s in range(m):
-            dec.truncate(s, base[s])
-    dec.sync()
-    stage, kname, kbytes = dominant_kernel(w, m)
-    cap = torch.cuda.Stream()
-    graph = torch.cuda.CUDAGraph()
-    dec.set_stream(cap)
-    with torch.cuda.graph(graph, stream=cap):
-        for l in range(w.layers):
-            dec.launch_stage(l, stage, m)
-    dec.set_stream(None)
-    graph.replay()
-    torch.cuda.synchronize()
-    durs = []
-    for _ in range(args.kernel_rounds):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+    # ---- the dominant kernel ----------------------------------------------------------------
+    kpl = dec.kernels_per_step(m)
+    if kpl == 1:
+        # the persistent step kernel is the whole step: its launches are the timed region's
+        kname = "persistent step kernel (k_step: all layers' GEMVs, attention, merge, output)"
+        kbytes = nb
+        k_ms = ms_step
+    else:
+        # one launch per layer captured in a CUDA graph (no host launch cost in the timing),
+        # replayed between CUDA events on the replay stream
+        if talker:
+            for s in range(m):
+                dec.truncate(s, base[s])
+        dec.sync()
+        stage, kname, kbytes = dominant_kernel(w, m)
+        cap = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        dec.set_stream(cap)
+        with torch.cuda.graph(graph, stream=cap):
+            for l in range(w.layers):
+                dec.launch_stage(l, stage, m)
+        dec.set_stream(None)
         graph.replay()
-        b.record(stream)
         torch.cuda.synchronize()
-        durs.append(a.elapsed_time(b) / w.layers)
-    del graph
-    k_ms = statistics.median(durs)
+        durs = []
+        for _ in range(args.kernel_rounds):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            durs.append(a.elapsed_time(b) / w.layers)
+        del graph
+        k_ms = statistics.median(durs)
     k_gbs = kbytes / (k_ms * 1e-3) / 1e9
     sha = kernel_source_sha()
     tr = NCU_TRAFFIC.get(w.name)
@@ -398,7 +421,8 @@ def run_ours(args):
            "l2": ("no flush: per-step working set %.2f GB >> 129 MB L2" % (nb / 1e9)
                   if nb > 4 * 129e6 else
                   "per-step working set %.1f MB may be partly L2-resident" % (nb / 1e6)),
-           "graph": "one CUDA graph per step, 6 PDL-chained kernels per layer + 1",
+           "graph": ("one CUDA graph per step holding one cooperative persistent kernel" if kpl == 1
+                     else "one CUDA graph per step, 6 PDL-chained kernels per layer + 1"),
            "parallelism": f"replicas x{world}"}
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,

@@ -50,6 +50,9 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1 } dec_dtype;
 /* flags */
 #define DEC_FLAG_TAPS 1u     /* keep the residual stream after every layer (dec_read_tap) */
 #define DEC_FLAG_NO_GRAPH 2u /* launch kernels one by one instead of replaying a CUDA graph */
+#define DEC_FLAG_PERSISTENT 4u /* steps of m <= 2 rows run as one persistent cooperative kernel
+                                  whose phases are separated by grid-wide barriers, instead of
+                                  the default chain of kernels; same results, bit for bit */
 
 /*
  * Model geometry.  Talker fields follow the talker's Dims (Qwen3-TTS talker on wgpu, `Dims`
@@ -152,7 +155,9 @@ dec_status dec_prefill_kv(dec_ctx* ctx, int stream, const float* k, const float*
  * Asynchronous: enqueued on the context's stream, returns without waiting; x_in must not
  * change and hidden_out must not be read until the stream reaches this point.  The first
  * step with a given (m, x_in, hidden_out) captures a CUDA graph (milliseconds); later steps
- * replay it.  Lengths advance by one on success; nothing changes on an error. */
+ * replay it (up to 8 graphs are kept; with DEC_FLAG_PERSISTENT and m <= 2 one graph per m
+ * serves every x_in / hidden_out pair).  Lengths advance by one on success; nothing changes on
+ * an error. */
 dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, float* hidden_out);
 
 /* dec_step with HOST buffers, blocking, as the talker page's step() returns its hidden state
@@ -184,7 +189,8 @@ dec_status dec_read_kv(dec_ctx* ctx, int layer, int stream, int position, float*
  * [m][hidden] f32 (the pages' stage probes, Mimi on wgpu, debug_read()).  Synchronous. */
 dec_status dec_read_tap(dec_ctx* ctx, int layer, int m, float* dst_host);
 
-/* Number of CUDA kernels one step of m rows launches (for launch accounting). */
+/* Number of CUDA kernels one step of m rows launches (for launch accounting): 6 * layers + 1,
+ * or 1 when the persistent kernel serves the step (DEC_FLAG_PERSISTENT, m <= 2). */
 int dec_kernels_per_step(const dec_ctx* ctx, int m);
 
 /* Talker only: shorten stream `stream` to `new_len` positions (0 <= new_len <= its length), so

@@ -91,6 +91,13 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
     return pol;
 }
 
+// Order this thread's earlier generic-proxy accesses to shared memory before later async-proxy
+// (bulk copy) accesses: needed before a bulk copy overwrites shared memory that threads have read
+// or written since the previous copy.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- loads ---------------------------------------------------------------------------------
 // Streaming 16-byte load of data that is read once (weights): bypass L1 allocation.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {

@@ -26,6 +26,7 @@
 #include <vector>
 
 #include "../../include/dec.h"
+#include "gemv_rows.cuh"
 #include "kernels.h"
 
 using namespace dec;
@@ -43,11 +44,18 @@ struct LayerW {
     const float *ln1_w, *ln1_b, *ln2_w, *ln2_b, *ls1, *ls2;
 };
 
-struct GraphEntry {
+// A step plan.  Persistent plans (phases != null) serve every input/output pair of their m: the
+// pointers are arguments of the graph's single kernel node, updated in place when they change.
+// Multi-kernel plans are per (m, input, output) triple.  exec is null with DEC_FLAG_NO_GRAPH.
+struct PlanEntry {
     int m;
     const float* x_in;
     float* out;
+    StepPhase* phases;       // device, or null (multi-kernel plan)
     cudaGraphExec_t exec;
+    cudaGraph_t graph;       // persistent plan: the captured graph, owner of `node`
+    cudaGraphNode_t node;    // persistent plan: the kernel node
+    cudaKernelNodeParams kp; // its launch parameters (kernelParams points at a StepParams)
 };
 
 constexpr size_t kAlign = 256;
@@ -66,6 +74,7 @@ cudaError_t configure_kernels() {
     if (dev < 64 && (done >> dev & 1u)) return cudaSuccess;
     if ((e = gemv_configure()) != cudaSuccess) return e;
     if ((e = attention_configure()) != cudaSuccess) return e;
+    if ((e = step_configure()) != cudaSuccess) return e;
     if (dev < 64) done |= (uint64_t)1 << dev;
     return cudaSuccess;
 }
@@ -91,6 +100,7 @@ struct dec_ctx {
     int slots = 0;          // KV rows per (layer, stream, kv head)
     int qkv_rows = 0;       // rows of the fused q/k/v matrix
     int max_chunks = 0;     // attention chunks per (stream, kv head)
+    int step_grid[3] = {};  // CTAs of the persistent step kernel for m = 1, 2 (0: not used)
     char* arena = nullptr;  // weights
     std::vector<LayerW> L;
     const float* final_norm = nullptr;
@@ -102,11 +112,12 @@ struct dec_ctx {
     float *part = nullptr, *part_ml = nullptr;  // attention chunk partials
     int32_t* len_dev = nullptr;
     unsigned* status = nullptr;
+    GridBarrier* gbar = nullptr;  // the persistent kernel's grid barrier
     float* taps = nullptr;
     float *io_in = nullptr, *io_out = nullptr;
     unsigned* status_host = nullptr;  // pinned
     std::vector<int> len_host;
-    std::vector<GraphEntry> graphs;
+    std::vector<PlanEntry> plans;
     std::string err;
 };
 
@@ -195,14 +206,24 @@ void build_rope_tables(int max_pos, int d, double theta, std::vector<float>& c,
         }
 }
 
-void destroy_graphs(dec_ctx* ctx) {
-    for (auto& g : ctx->graphs) cudaGraphExecDestroy(g.exec);
-    ctx->graphs.clear();
+void destroy_plan(PlanEntry& e) {
+    if (e.exec) cudaGraphExecDestroy(e.exec);
+    if (e.graph) cudaGraphDestroy(e.graph);
+    if (e.phases) cudaFree(e.phases);
+    e.exec = nullptr;
+    e.graph = nullptr;
+    e.phases = nullptr;
 }
 
-// Launch kernel `stage` of layer `l` for rows 0..m-1 (see dec_launch_stage for the stages).
-cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_in, cudaStream_t s,
-                         bool pdl) {
+void destroy_plans(dec_ctx* ctx) {
+    for (auto& e : ctx->plans) destroy_plan(e);
+    ctx->plans.clear();
+}
+
+// Parameters of stage `stage` of layer `l` for rows 0..m-1 (see dec_launch_stage for the
+// stages): a GEMV (returns false) or, for stage 1, the attention (returns true; `a` is filled).
+bool stage_params(dec_ctx* ctx, int l, int stage, int m, const float* x_in, GemvParams& g,
+                  AttnParams& a) {
     const dec_config& c = ctx->cfg;
     const bool talker = c.kind == DEC_QWEN3_TALKER;
     const int h = c.hidden, d = c.head_dim, H = c.q_heads, G = c.kv_heads, I = c.inter;
@@ -211,10 +232,11 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
     const size_t kv_layer = (size_t)S * G * ctx->slots * d;
     const LayerW& W = ctx->L[l];
     const float* xr = (l == 0) ? x_in : ctx->xres;  // residual stream entering layer l
-    GemvParams g = {};
+    g = GemvParams{};
     g.m = m;
     g.eps = c.norm_eps;
     g.status = ctx->status;
+    g.unit = 1;
     switch (stage) {
         case 0:  // norm + q/k/v
             g.W = talker ? W.qkv : W.in_proj;
@@ -228,9 +250,9 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
             g.epi = EPI_STORE;
             g.y = ctx->qkv;
             g.ldy = ctx->qkv_rows;
-            return launch_gemv(g, c.weight_dtype, ctx->num_sms, s, pdl);
-        case 1: {  // attention with its prologue
-            AttnParams a = {};
+            return false;
+        case 1:  // attention with its prologue
+            a = AttnParams{};
             a.mode = talker ? ATTN_TALKER : ATTN_RING;
             a.m = m;
             a.H = H;
@@ -252,14 +274,11 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
             a.max_pos = c.max_pos;
             a.part = ctx->part;
             a.part_ml = ctx->part_ml;
-            a.tickets = nullptr;  // partials are merged by the merge kernel below
+            a.tickets = nullptr;  // partials are merged by the merge kernel / phase
             a.max_chunks = ctx->max_chunks;
             a.out = ctx->attn;
             a.status = ctx->status;
-            cudaError_t e = launch_attention(a, s, pdl);
-            if (e != cudaSuccess) return e;
-            return launch_attention_merge(a, s, true);
-        }
+            return true;
         case 2:  // o-proj + residual (codec: LayerScale)
             g.W = talker ? W.o : W.out_proj;
             g.N = h;
@@ -273,7 +292,7 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
             g.res = xr;
             g.ldres = h;
             g.ls = talker ? nullptr : W.ls1;
-            return launch_gemv(g, c.weight_dtype, ctx->num_sms, s, pdl);
+            return false;
         case 3:  // norm + gate/up + SwiGLU (codec: lin1 + GELU)
             g.W = talker ? W.gu : W.lin1;
             g.N = talker ? 2 * I : I;
@@ -284,10 +303,11 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
             g.nw = talker ? W.post_norm : W.ln2_w;
             g.nb = talker ? nullptr : W.ln2_b;
             g.epi = talker ? EPI_SWIGLU : EPI_GELU;
+            g.unit = talker ? 2 : 1;
             g.y = ctx->act;
             g.ldy = I;
-            return launch_gemv(g, c.weight_dtype, ctx->num_sms, s, pdl);
-        case 4:  // down + residual (codec: lin2 + LayerScale)
+            return false;
+        default:  // 4: down + residual (codec: lin2 + LayerScale)
             g.W = talker ? W.down : W.lin2;
             g.N = h;
             g.K = I;
@@ -302,23 +322,26 @@ cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_i
             g.ls = talker ? nullptr : W.ls2;
             g.tap = ctx->taps ? ctx->taps + (size_t)l * S * h : nullptr;
             g.ldtap = h;
-            return launch_gemv(g, c.weight_dtype, ctx->num_sms, s, pdl);
-        default:
-            return cudaErrorInvalidValue;
+            return false;
     }
 }
 
-// Enqueue the kernels of one step on `s`: five per layer, then the final kernel.  Every
-// kernel but the step's first is launched as a programmatic dependent of its predecessor.
-cudaError_t enqueue_step(dec_ctx* ctx, int m, const float* x_in, float* out, cudaStream_t s,
-                         bool first_pdl) {
+// Launch stage `stage` of layer `l` for rows 0..m-1: one GEMV kernel, or for stage 1 the
+// attention chunks and the merge of their partials.
+cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_in, cudaStream_t s,
+                         bool pdl) {
+    if (stage < 0 || stage > 4) return cudaErrorInvalidValue;
+    GemvParams g;
+    AttnParams a;
+    if (!stage_params(ctx, l, stage, m, x_in, g, a))
+        return launch_gemv(g, ctx->cfg.weight_dtype, ctx->num_sms, s, pdl);
+    cudaError_t e = launch_attention(a, s, pdl);
+    if (e != cudaSuccess) return e;
+    return launch_attention_merge(a, s, true);
+}
+
+FinalParams final_params(dec_ctx* ctx, int m, float* out) {
     const dec_config& c = ctx->cfg;
-    cudaError_t e;
-    for (int l = 0; l < c.layers; ++l)
-        for (int stage = 0; stage < 5; ++stage)
-            if ((e = launch_stage(ctx, l, stage, m, x_in, s,
-                                  first_pdl || l > 0 || stage > 0)) != cudaSuccess)
-                return e;
     FinalParams f = {};
     f.m = m;
     f.h = c.hidden;
@@ -327,32 +350,149 @@ cudaError_t enqueue_step(dec_ctx* ctx, int m, const float* x_in, float* out, cud
     f.eps = c.norm_eps;
     f.out = out;
     f.len = ctx->len_dev;
-    return launch_final(f, s, true);
+    return f;
 }
 
-cudaGraphExec_t get_graph(dec_ctx* ctx, int m, const float* x_in, float* out, cudaError_t* err) {
-    for (auto& g : ctx->graphs)
-        if (g.m == m && g.x_in == x_in && g.out == out) return g.exec;
-    *err = cudaStreamBeginCapture(ctx->cap_stream, cudaStreamCaptureModeThreadLocal);
-    if (*err != cudaSuccess) return nullptr;
-    cudaError_t e = enqueue_step(ctx, m, x_in, out, ctx->cap_stream, false);
-    cudaGraph_t graph = nullptr;
-    cudaError_t e2 = cudaStreamEndCapture(ctx->cap_stream, &graph);
-    if (e != cudaSuccess || e2 != cudaSuccess) {
-        if (graph) cudaGraphDestroy(graph);
-        *err = e != cudaSuccess ? e : e2;
-        return nullptr;
+// The persistent kernel's phase list of a step (per layer: QKV, attention, merge, o-proj,
+// gate/up, down; then the output rows).  Each CTA starts staging layer 0's K/V chunk in the
+// first phase and layer l+1's in layer l's o-proj phase.  Empty when some GEMV of the plan is
+// not served by the split-K GEMV.
+std::vector<StepPhase> build_phases(dec_ctx* ctx, int m) {
+    const dec_config& c = ctx->cfg;
+    std::vector<StepPhase> ph;
+    ph.reserve((size_t)6 * c.layers + 1);
+    for (int l = 0; l < c.layers; ++l) {
+        for (int stage = 0; stage < 5; ++stage) {
+            StepPhase p = {};
+            p.stage_attn = -1;
+            // layer 0 reads the step input: its pointer is a kernel argument (StepIo)
+            if (l == 0 && stage == 0) p.io = IO_X;
+            if (l == 0 && stage == 2) p.io = IO_RES;
+            if (stage_params(ctx, l, stage, m, nullptr, p.g, p.a)) {
+                p.type = PH_ATTN;
+                ph.push_back(p);
+                p.type = PH_MERGE;
+                ph.push_back(p);
+                continue;
+            }
+            p.type = PH_GEMV;
+            p.nj = rows_gemv_nj(p.g.K, m, c.weight_dtype);
+            if (!p.nj) return {};
+            if (stage == 0 && l == 0) p.stage_attn = 1;
+            if (stage == 2 && l + 1 < c.layers) p.stage_attn = 6 * (l + 1) + 1;
+            ph.push_back(p);
+        }
     }
-    cudaGraphExec_t exec = nullptr;
-    *err = cudaGraphInstantiate(&exec, graph, 0);
-    cudaGraphDestroy(graph);
-    if (*err != cudaSuccess) return nullptr;
-    if (ctx->graphs.size() >= 8) {
-        cudaGraphExecDestroy(ctx->graphs.front().exec);
-        ctx->graphs.erase(ctx->graphs.begin());
+    for (StepPhase& p : ph)
+        if (p.stage_attn >= 0) {
+            p.stage_kc = ph[p.stage_attn].a.kc;
+            p.stage_vc = ph[p.stage_attn].a.vc;
+        }
+    StepPhase f = {};
+    f.type = PH_FINAL;
+    f.stage_attn = -1;
+    f.io = IO_OUT;
+    f.f = final_params(ctx, m, nullptr);
+    ph.push_back(f);
+    return ph;
+}
+
+// Enqueue the multi-kernel plan of one step on `s`: six kernels per layer, then the final
+// kernel.  Every kernel but the step's first is launched as a programmatic dependent of its
+// predecessor.
+cudaError_t enqueue_kernels(dec_ctx* ctx, int m, const float* x_in, float* out, cudaStream_t s) {
+    const dec_config& c = ctx->cfg;
+    cudaError_t e;
+    for (int l = 0; l < c.layers; ++l)
+        for (int stage = 0; stage < 5; ++stage)
+            if ((e = launch_stage(ctx, l, stage, m, x_in, s, l > 0 || stage > 0)) != cudaSuccess)
+                return e;
+    return launch_final(final_params(ctx, m, out), s, true);
+}
+
+StepParams step_params(dec_ctx* ctx, const StepPhase* phases, const float* x_in, float* out) {
+    StepParams sp = {};
+    sp.phases = phases;
+    sp.n_phases = 6 * ctx->cfg.layers + 1;
+    sp.attn0 = 1;
+    sp.bar = ctx->gbar;
+    sp.status = ctx->status;
+    sp.x_in = x_in;
+    sp.out = out;
+    return sp;
+}
+
+// Enqueue one step of a plan: the persistent kernel when the plan has a phase list, else the
+// kernels one by one.
+cudaError_t enqueue_step(dec_ctx* ctx, const PlanEntry& pe, const float* x_in, float* out,
+                         cudaStream_t s) {
+    if (!pe.phases) return enqueue_kernels(ctx, pe.m, x_in, out, s);
+    return launch_step(step_params(ctx, pe.phases, x_in, out), ctx->cfg.weight_dtype, pe.m,
+                       ctx->cfg.head_dim, ctx->step_grid[pe.m], s);
+}
+
+bool uses_persistent(const dec_ctx* ctx, int m) {
+    return m >= 1 && m <= 2 && ctx->step_grid[m] > 0;
+}
+
+// The plan for (m, x_in, out): found in the cache or built (phase list uploaded, graph captured).
+PlanEntry* get_plan(dec_ctx* ctx, int m, const float* x_in, float* out, cudaError_t* err) {
+    for (auto& e : ctx->plans)
+        if (e.m == m && (e.phases || (e.x_in == x_in && e.out == out))) return &e;
+    PlanEntry pe = {};
+    pe.m = m;
+    pe.x_in = x_in;
+    pe.out = out;
+    if (uses_persistent(ctx, m)) {
+        const std::vector<StepPhase> ph = build_phases(ctx, m);
+        if (!ph.empty()) {
+            const size_t bytes = ph.size() * sizeof(StepPhase);
+            if ((*err = cudaMalloc(&pe.phases, bytes)) != cudaSuccess) return nullptr;
+            if ((*err = cudaMemcpy(pe.phases, ph.data(), bytes, cudaMemcpyHostToDevice)) != cudaSuccess) {
+                destroy_plan(pe);
+                return nullptr;
+            }
+        }
     }
-    ctx->graphs.push_back({m, x_in, out, exec});
-    return exec;
+    if (!(ctx->cfg.flags & DEC_FLAG_NO_GRAPH)) {
+        *err = cudaStreamBeginCapture(ctx->cap_stream, cudaStreamCaptureModeThreadLocal);
+        if (*err != cudaSuccess) {
+            destroy_plan(pe);
+            return nullptr;
+        }
+        cudaError_t e = enqueue_step(ctx, pe, x_in, out, ctx->cap_stream);
+        cudaGraph_t graph = nullptr;
+        cudaError_t e2 = cudaStreamEndCapture(ctx->cap_stream, &graph);
+        if (e != cudaSuccess || e2 != cudaSuccess) {
+            if (graph) cudaGraphDestroy(graph);
+            *err = e != cudaSuccess ? e : e2;
+            destroy_plan(pe);
+            return nullptr;
+        }
+        if (pe.phases) {  // the single kernel node, for in-place pointer updates
+            size_t n = 1;
+            *err = cudaGraphGetNodes(graph, &pe.node, &n);
+            if (*err == cudaSuccess && n != 1) *err = cudaErrorInvalidValue;
+            if (*err == cudaSuccess) *err = cudaGraphKernelNodeGetParams(pe.node, &pe.kp);
+        }
+        if (*err == cudaSuccess) *err = cudaGraphInstantiate(&pe.exec, graph, 0);
+        if (pe.phases)
+            pe.graph = graph;  // keeps the node handle valid for updates
+        else
+            cudaGraphDestroy(graph);
+        if (*err != cudaSuccess) {
+            destroy_plan(pe);
+            return nullptr;
+        }
+    }
+    if (ctx->plans.size() >= 8) {
+        // a graph still queued on the stream is freed when it completes; a phase list is not
+        // (cudaFree waits for the device)
+        destroy_plan(ctx->plans.front());
+        ctx->plans.erase(ctx->plans.begin());
+    }
+    ctx->plans.push_back(pe);
+    return &ctx->plans.back();
 }
 
 dec_status check_step_args(dec_ctx* ctx, int m, const int32_t* pos) {
@@ -373,16 +513,23 @@ dec_status check_step_args(dec_ctx* ctx, int m, const int32_t* pos) {
 }
 
 dec_status run_step(dec_ctx* ctx, int m, const float* x_in, float* out) {
-    if (ctx->cfg.flags & DEC_FLAG_NO_GRAPH) {
-        cudaError_t e = enqueue_step(ctx, m, x_in, out, ctx->stream, false);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "step launch");
-    } else {
-        cudaError_t e = cudaSuccess;
-        cudaGraphExec_t exec = get_graph(ctx, m, x_in, out, &e);
-        if (!exec) return cuda_fail(ctx, e, "step graph capture");
-        e = cudaGraphLaunch(exec, ctx->stream);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "graph launch");
+    cudaError_t e = cudaSuccess;
+    PlanEntry* pe = get_plan(ctx, m, x_in, out, &e);
+    if (!pe) return cuda_fail(ctx, e, "step plan");
+    if (pe->exec && pe->phases && (pe->x_in != x_in || pe->out != out)) {
+        // new input/output buffers: update the kernel node's arguments in place
+        StepParams sp = step_params(ctx, pe->phases, x_in, out);
+        void* args[] = {&sp};
+        cudaKernelNodeParams kp = pe->kp;
+        kp.kernelParams = args;
+        kp.extra = nullptr;
+        e = cudaGraphExecKernelNodeSetParams(pe->exec, pe->node, &kp);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "step graph update");
+        pe->x_in = x_in;
+        pe->out = out;
     }
+    e = pe->exec ? cudaGraphLaunch(pe->exec, ctx->stream) : enqueue_step(ctx, *pe, x_in, out, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "step launch");
     for (int i = 0; i < m; ++i) ctx->len_host[i] += 1;
     return DEC_OK;
 }
@@ -392,6 +539,8 @@ dec_status read_status(dec_ctx* ctx) {
     if (st == 0) return DEC_OK;
     *ctx->status_host = 0;
     cudaMemset(ctx->status, 0, sizeof(unsigned));
+    // a barrier wait that gave up leaves the grid barrier mid-count: start it over (nothing runs)
+    if ((st & CHECK_WAIT_LIMIT) && ctx->gbar) cudaMemset(ctx->gbar, 0, sizeof(GridBarrier));
     return fail(ctx, DEC_E_DEVICE_CHECK, "device check fired:%s%s",
                 (st & CHECK_WAIT_LIMIT) ? " wait-limit" : "", (st & CHECK_BOUNDS) ? " bounds" : "");
 }
@@ -454,6 +603,9 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     cudaError_t e = configure_kernels();
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "kernel attributes"));
     ctx->max_chunks = (ctx->slots + kAttnChunk - 1) / kAttnChunk;
+    if (c.flags & DEC_FLAG_PERSISTENT)
+        for (int mm = 1; mm <= std::min(2, ctx->S); ++mm)
+            ctx->step_grid[mm] = step_grid(c.weight_dtype, mm, d, ctx->num_sms);
     e = cudaStreamCreateWithFlags(&ctx->cap_stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "capture stream"));
     if ((e = cudaMallocHost(&ctx->status_host, sizeof(unsigned))) != cudaSuccess)
@@ -566,7 +718,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     const size_t o_att = take((size_t)S * qw * 4), o_act = take((size_t)S * I * 4);
     const size_t o_part = take(attention_part_bytes(S, H, ctx->max_chunks, d));
     const size_t o_ml = take(attention_ml_bytes(S, H, ctx->max_chunks));
-    const size_t o_len = take((size_t)S * 4), o_st = take(4);
+    const size_t o_len = take((size_t)S * 4), o_st = take(4), o_gbar = take(sizeof(GridBarrier));
     const size_t o_taps = (c.flags & DEC_FLAG_TAPS) ? take((size_t)c.layers * S * h * 4) : 0;
     const size_t o_in = take((size_t)S * h * 4), o_out = take((size_t)S * h * 4);
     if ((e = cudaMalloc(&ctx->state, tot)) != cudaSuccess) return bail(cuda_fail(ctx, e, "state"));
@@ -584,6 +736,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->part_ml = reinterpret_cast<float*>(b + o_ml);
     ctx->len_dev = reinterpret_cast<int32_t*>(b + o_len);
     ctx->status = reinterpret_cast<unsigned*>(b + o_st);
+    ctx->gbar = reinterpret_cast<GridBarrier*>(b + o_gbar);
     ctx->taps = (c.flags & DEC_FLAG_TAPS) ? reinterpret_cast<float*>(b + o_taps) : nullptr;
     ctx->io_in = reinterpret_cast<float*>(b + o_in);
     ctx->io_out = reinterpret_cast<float*>(b + o_out);
@@ -608,7 +761,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
 void dec_destroy(dec_ctx* ctx) {
     if (!ctx) return;
     if (ctx->stream || ctx->cap_stream) cudaStreamSynchronize(ctx->stream);
-    destroy_graphs(ctx);
+    destroy_plans(ctx);
     if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
     if (ctx->arena) cudaFree(ctx->arena);
     if (ctx->state) cudaFree(ctx->state);
@@ -754,6 +907,12 @@ dec_status dec_read_tap(dec_ctx* ctx, int layer, int m, float* dst_host) {
 
 int dec_kernels_per_step(const dec_ctx* ctx, int m) {
     if (!ctx || m < 1 || m > ctx->S) return -1;
+    if (uses_persistent(ctx, m)) {
+        // the persistent kernel serves the plan unless one of its GEMVs is too wide for it
+        const int wide = std::max(std::max(ctx->cfg.hidden, ctx->cfg.inter),
+                                  ctx->cfg.q_heads * ctx->cfg.head_dim);
+        if (rows_gemv_nj(wide, m, ctx->cfg.weight_dtype)) return 1;
+    }
     return 6 * ctx->cfg.layers + 1;
 }
 

@@ -16,6 +16,7 @@
 // (the talker's ADD after o/down, Mimi MV_LS); SwiGLU over interleaved gate/up rows (SWIGLU_SRC);
 // GELU(erf) (GELU_ERF, with CUDA's erff).
 #include "common.cuh"
+#include "gemv_rows.cuh"
 #include "kernels.h"
 
 namespace dec {
@@ -24,19 +25,6 @@ constexpr int kGemvThreads = 256;
 constexpr int kGemvWarps = kGemvThreads / 32;
 constexpr int kRows = 2;     // rows per warp task (a gate/up pair for SwiGLU)
 constexpr int kUnroll = 4;   // 16-byte steps per row in flight
-
-template <int DT>
-struct WT;
-template <>
-struct WT<0> {  // f32 weights
-    static constexpr int VEC = 4;
-    static constexpr int ES = 4;
-};
-template <>
-struct WT<1> {  // bf16 weights
-    static constexpr int VEC = 8;
-    static constexpr int ES = 2;
-};
 
 // Shared-memory position of x element k.  For bf16 a lane consumes 8 consecutive k per step;
 // storing each 256-wide block as [half][lane][4] lets the lane fetch its 8 values with two
@@ -49,19 +37,14 @@ __device__ __forceinline__ int sx_index(int k) {
     return blk + ((j >> 2) << 7) + (l << 2) + (j & 3);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
-__device__ __forceinline__ float gelu_f(float v) {
-    return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
-}
-
 template <int DT, int MT>
 __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv(const GemvParams p) {
     extern __shared__ __align__(16) float sx[];  // [m][ldsx]
     __shared__ float red[kGemvWarps][MT];
     __shared__ float stat[2][MT];
 
-    constexpr int VEC = WT<DT>::VEC;
-    constexpr int ES = WT<DT>::ES;
+    constexpr int VEC = WType<DT>::VEC;
+    constexpr int ES = WType<DT>::ES;
     constexpr int KS = 32 * VEC;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int N = p.N, K = p.K, m = p.m;
@@ -257,255 +240,18 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv(const GemvParams p) {
 }
 
 // =============================================================================================
-// Split-K row-streaming GEMV for m <= 2 (the decode step's common case).
-//
-// All 256 threads of a CTA split K: warp w, lane l owns the 16-byte weight granules
-// g = (8 j + w) 32 + l (j < NJ), so each warp-wide load is 512 contiguous bytes of one row and
-// the CTA's threads together cover a whole row.  A thread's slice of x is only NJ granules wide,
-// so x lives in registers, loaded once; the norm prologue is a block reduction over those
-// registers (no shared-memory staging).  The CTA's rows are streamed in batches of RB rows with
-// the next batch's loads in flight while the current one is consumed (double-buffered
-// registers); the first batch is issued before griddepcontrol.wait.  Per batch, each warp folds
-// its RB row partials across lanes with a transposed butterfly (lanes 4r..4r+3 end up holding
-// row r), and the cross-warp sum plus the epilogue run once at the end of the CTA.
+// Split-K row-streaming GEMV for m <= 2 (the decode step's common case), on its own: the first
+// two weight batches are issued before griddepcontrol.wait (see gemv_rows.cuh).
 // =============================================================================================
-constexpr int kRowsThreads = 256;
-constexpr int kRowsWarps = kRowsThreads / 32;
-constexpr int kRowsMaxRows = 64;  // rows per CTA the cross-warp scratch holds
-
-// v[0..7] per lane -> lane l returns the warp-wide sum of v[(l >> 2) & 7]
-__device__ __forceinline__ float butterfly8(float v[8], int lane) {
-    const bool hi16 = lane & 16, hi8 = lane & 8, hi4 = lane & 4;
-    float a[4], b[2];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = hi16 ? v[i] : v[i + 4];
-        const float keep = hi16 ? v[i + 4] : v[i];
-        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = hi8 ? a[i] : a[i + 2];
-        const float keep = hi8 ? a[i + 2] : a[i];
-        b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    const float send = hi4 ? b[0] : b[1];
-    float c = (hi4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    c += __shfl_xor_sync(0xffffffffu, c, 2);
-    c += __shfl_xor_sync(0xffffffffu, c, 1);
-    return c;
-}
-
 template <int DT, int MT, int NJ>
 __global__ void __launch_bounds__(kRowsThreads, 2) k_gemv_rows(const GemvParams p) {
-    constexpr int VEC = WT<DT>::VEC;
-    constexpr int ES = WT<DT>::ES;
-    constexpr int RB = NJ >= 8 ? 1 : 8 / NJ;   // rows per batch (8 loads per lane in flight)
-    __shared__ float red[kRowsWarps][kRowsMaxRows][MT];
-    __shared__ float nred[kRowsWarps][MT];
-    __shared__ float stat[2][MT];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = p.K, m = p.m;
-    const int G = K / VEC;
-    const size_t row_bytes = (size_t)K * ES;
-    const int units = p.N / p.unit;
-    const int u0 = (int)((long long)blockIdx.x * units / gridDim.x);
-    const int u1 = (int)((long long)(blockIdx.x + 1) * units / gridDim.x);
-    const int row0 = u0 * p.unit, nrows = (u1 - u0) * p.unit;
-    const char* Wb = static_cast<const char*>(p.W) + (size_t)row0 * row_bytes;
-
-    int gj[NJ];
-    bool ok[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        gj[j] = (j * kRowsWarps + warp) * 32 + lane;
-        ok[j] = gj[j] < G;
-    }
-    const uint64_t pol = l2_evict_first();
-    uint4 wa[RB][NJ], wb[RB][NJ];
-    auto load = [&](uint4 (&w)[RB][NJ], int b0) {
-#pragma unroll
-        for (int r = 0; r < RB; ++r)
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-                w[r][j] = (b0 + r < nrows && ok[j])
-                              ? ld_stream16(Wb + (size_t)(b0 + r) * row_bytes + (size_t)gj[j] * 16, pol)
-                              : make_uint4(0u, 0u, 0u, 0u);
-    };
-
-    // weights first: independent of the previous kernel, so two batches are in flight before
-    // the wait (a whole CTA's rows when it owns at most 2 * RB of them)
-    load(wa, 0);
-    load(wb, RB);
+    __shared__ float sh[rows_smem_floats<MT>()];
+    using R = RowsGemv<DT, MT, NJ, 8>;
+    uint4 wa[8], wb[8];
+    R::issue(p, blockIdx.x, gridDim.x, wa, wb);
     pdl_trigger();
     pdl_wait();
-
-    // ---- x slice in registers, norm prologue as a block reduction ---------------------------
-    float2 xv[MT][NJ][VEC / 2];
-#pragma unroll
-    for (int mm = 0; mm < MT; ++mm)
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const float* src = p.x + (size_t)mm * p.ldx + (size_t)gj[j] * VEC;
-#pragma unroll
-            for (int q = 0; q < VEC / 4; ++q) {
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (mm < m && ok[j]) a = *reinterpret_cast<const float4*>(src + 4 * q);
-                xv[mm][j][2 * q] = make_float2(a.x, a.y);
-                xv[mm][j][2 * q + 1] = make_float2(a.z, a.w);
-            }
-        }
-    if (p.pro != PRO_NONE) {
-        auto block_sum = [&](float (&v)[MT], int slot) {
-#pragma unroll
-            for (int mm = 0; mm < MT; ++mm) {
-                const float t = warp_sum(v[mm]);
-                if (lane == 0) nred[warp][mm] = t;
-            }
-            __syncthreads();
-            if (tid < MT) {
-                float sum = 0.f;
-                for (int w = 0; w < kRowsWarps; ++w) sum += nred[w][tid];
-                stat[slot][tid] = sum / (float)K;
-            }
-            __syncthreads();
-        };
-        float part[MT];
-#pragma unroll
-        for (int mm = 0; mm < MT; ++mm) {
-            part[mm] = 0.f;
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-#pragma unroll
-                for (int e = 0; e < VEC / 2; ++e) {
-                    const float2 v = xv[mm][j][e];
-                    part[mm] += (p.pro == PRO_LN) ? v.x + v.y : v.x * v.x + v.y * v.y;
-                }
-        }
-        block_sum(part, 0);  // mean (LayerNorm) or mean square (RMSNorm)
-        float inv[MT], mean[MT];
-        if (p.pro == PRO_LN) {
-#pragma unroll
-            for (int mm = 0; mm < MT; ++mm) {
-                mean[mm] = stat[0][mm];
-                part[mm] = 0.f;
-#pragma unroll
-                for (int j = 0; j < NJ; ++j)
-#pragma unroll
-                    for (int e = 0; e < VEC / 2; ++e) {
-                        if (!ok[j]) continue;
-                        const float dx = xv[mm][j][e].x - mean[mm], dy = xv[mm][j][e].y - mean[mm];
-                        part[mm] += dx * dx + dy * dy;
-                    }
-            }
-            block_sum(part, 1);
-#pragma unroll
-            for (int mm = 0; mm < MT; ++mm) inv[mm] = 1.0f / sqrtf(stat[1][mm] + p.eps);
-        } else {
-#pragma unroll
-            for (int mm = 0; mm < MT; ++mm) {
-                mean[mm] = 0.f;
-                inv[mm] = 1.0f / sqrtf(stat[0][mm] + p.eps);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            if (!ok[j]) continue;
-            const int k0 = gj[j] * VEC;
-#pragma unroll
-            for (int e = 0; e < VEC / 2; ++e) {
-                const float2 w = *reinterpret_cast<const float2*>(p.nw + k0 + 2 * e);
-                float2 b = make_float2(0.f, 0.f);
-                if (p.pro == PRO_LN) b = *reinterpret_cast<const float2*>(p.nb + k0 + 2 * e);
-#pragma unroll
-                for (int mm = 0; mm < MT; ++mm) {
-                    float2& v = xv[mm][j][e];
-                    v.x = (v.x - mean[mm]) * inv[mm] * w.x + b.x;
-                    v.y = (v.y - mean[mm]) * inv[mm] * w.y + b.y;
-                }
-            }
-        }
-    }
-
-    // ---- stream the CTA's rows in double-buffered batches --------------------------------------
-    auto consume = [&](const uint4 (&w)[RB][NJ], int b0) {
-        float part[MT][8];
-#pragma unroll
-        for (int mm = 0; mm < MT; ++mm)
-#pragma unroll
-            for (int r = 0; r < 8; ++r) part[mm][r] = 0.f;
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            float2 acc[MT];
-#pragma unroll
-            for (int mm = 0; mm < MT; ++mm) acc[mm] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                float2 wf[VEC / 2];
-                if constexpr (DT == 1) {
-                    wf[0] = bf16x2_to_f32x2(w[r][j].x);
-                    wf[1] = bf16x2_to_f32x2(w[r][j].y);
-                    wf[2] = bf16x2_to_f32x2(w[r][j].z);
-                    wf[3] = bf16x2_to_f32x2(w[r][j].w);
-                } else {
-                    wf[0] = make_float2(__uint_as_float(w[r][j].x), __uint_as_float(w[r][j].y));
-                    wf[1] = make_float2(__uint_as_float(w[r][j].z), __uint_as_float(w[r][j].w));
-                }
-#pragma unroll
-                for (int mm = 0; mm < MT; ++mm)
-#pragma unroll
-                    for (int e = 0; e < VEC / 2; ++e) acc[mm] = ffma2(wf[e], xv[mm][j][e], acc[mm]);
-            }
-#pragma unroll
-            for (int mm = 0; mm < MT; ++mm) part[mm][r] = acc[mm].x + acc[mm].y;
-        }
-#pragma unroll
-        for (int mm = 0; mm < MT; ++mm) {
-            const float v = butterfly8(part[mm], lane);
-            const int r = (lane >> 2) & 7;
-            if ((lane & 3) == 0 && r < RB && b0 + r < nrows) red[warp][b0 + r][mm] = v;
-        }
-    };
-    // ping-pong: while one batch is consumed the other is in flight
-    for (int b0 = 0; b0 < nrows; b0 += 2 * RB) {
-        consume(wa, b0);
-        if (b0 + 2 * RB < nrows) load(wa, b0 + 2 * RB);
-        if (b0 + RB < nrows) consume(wb, b0 + RB);
-        if (b0 + 3 * RB < nrows) load(wb, b0 + 3 * RB);
-    }
-    __syncthreads();
-
-    // ---- cross-warp sums and the epilogue --------------------------------------------------------
-    if (p.epi == EPI_SWIGLU) {
-        for (int t = tid; t < (nrows / 2) * m; t += kRowsThreads) {
-            const int pr = t / m, mm = t - pr * m;
-            float vg = 0.f, vu = 0.f;
-            for (int w = 0; w < kRowsWarps; ++w) {
-                vg += red[w][2 * pr][mm];
-                vu += red[w][2 * pr + 1][mm];
-            }
-            p.y[(size_t)mm * p.ldy + row0 / 2 + pr] = silu_f(vg) * vu;
-        }
-    } else {
-        for (int t = tid; t < nrows * m; t += kRowsThreads) {
-            const int r = t / m, mm = t - r * m;
-            float v = 0.f;
-            for (int w = 0; w < kRowsWarps; ++w) v += red[w][r][mm];
-            const int row = row0 + r;
-            float out;
-            if (p.epi == EPI_RESID) {
-                const float tt = p.ls ? p.ls[row] * v : v;
-                out = p.res[(size_t)mm * p.ldres + row] + tt;
-                if (p.tap) p.tap[(size_t)mm * p.ldtap + row] = out;
-            } else if (p.epi == EPI_GELU) {
-                out = gelu_f(v);
-            } else {
-                out = v;
-            }
-            p.y[(size_t)mm * p.ldy + row] = out;
-        }
-    }
+    R::run(p, blockIdx.x, gridDim.x, wa, wb, sh);
 }
 
 size_t gemv_smem_bytes(int m, int K) {
@@ -516,7 +262,7 @@ size_t gemv_smem_bytes(int m, int K) {
 
 template <int DT, int MT>
 static cudaError_t launch_t(const GemvParams& p, int num_sms, cudaStream_t s, bool pdl) {
-    constexpr int KS = 32 * WT<DT>::VEC;
+    constexpr int KS = 32 * WType<DT>::VEC;
     const int ldsx = ((p.K + KS - 1) / KS) * KS;
     const size_t smem = (size_t)p.m * ldsx * sizeof(float);
     const int ngroups = (p.N + kRows - 1) / kRows;
@@ -559,7 +305,7 @@ template <int DT, int MT, int NJ>
 static cudaError_t launch_rows_t(GemvParams p, int num_sms, cudaStream_t s, bool pdl) {
     p.unit = p.epi == EPI_SWIGLU ? 2 : 1;
     const int units = p.N / p.unit;
-    int grid = 2 * num_sms;
+    int grid = (p.per_sm > 0 ? p.per_sm : 2) * num_sms;
     // at most kRowsMaxRows rows per CTA
     const int need = (p.N + kRowsMaxRows - 2) / (kRowsMaxRows - 1);
     if (grid < need) grid = need;
@@ -577,14 +323,6 @@ static cudaError_t launch_rows_t(GemvParams p, int num_sms, cudaStream_t s, bool
     return cudaLaunchKernelEx(&cfg, k_gemv_rows<DT, MT, NJ>, p);
 }
 
-// granules per lane of the split-K kernel (0: shape not served by it)
-static int rows_nj(const GemvParams& p, int dtype) {
-    const int vec = dtype == 1 ? 8 : 4;
-    const int per_pass = kRowsThreads * vec;  // elements one pass of the CTA covers
-    const int nj = (p.K + per_pass - 1) / per_pass;
-    return (p.m <= 2 && nj <= 4 && nj != 0) ? (nj == 3 ? 3 : nj == 4 ? 4 : nj) : 0;
-}
-
 template <int DT, int MT>
 static cudaError_t launch_rows_nj(const GemvParams& p, int nj, int num_sms, cudaStream_t s, bool pdl) {
     switch (nj) {
@@ -596,7 +334,7 @@ static cudaError_t launch_rows_nj(const GemvParams& p, int nj, int num_sms, cuda
 }
 
 cudaError_t launch_gemv(const GemvParams& p, int dtype, int num_sms, cudaStream_t s, bool pdl) {
-    const int nj = rows_nj(p, dtype);
+    const int nj = rows_gemv_nj(p.K, p.m, dtype);
     if (nj) {
         if (dtype == 1) return p.m <= 1 ? launch_rows_nj<1, 1>(p, nj, num_sms, s, pdl)
                                         : launch_rows_nj<1, 2>(p, nj, num_sms, s, pdl);

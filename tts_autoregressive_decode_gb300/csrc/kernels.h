@@ -44,11 +44,9 @@ struct GemvParams {
     float* tap;            // optional copy of y rows [m][ldtap] (EPI_RESID)
     int ldtap;
     unsigned* status;      // device check word (bounded waits), may be null
-    // filled by launch_gemv for the bulk-copy pipeline
-    int rb;                // rows per stage
-    int nstages;           // stages in the ring
     int unit;              // rows per partition unit (2 for SwiGLU pairs)
-    int stage_stride;      // bytes between ring stages
+    int per_sm;            // split-K GEMV launch: CTAs per SM (0: 2).  One CTA per SM leaves room
+                           // for the next kernel's CTAs to start and stage their loads early
 };
 
 // dtype: 0 f32, 1 bf16.  Launches with the programmatic-dependency attribute when pdl.
@@ -119,6 +117,54 @@ struct FinalParams {
     int32_t* len;          // [m]: incremented
 };
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
+
+// ---------------------------------------------------------------------------------------------
+// Persistent step kernel (m <= 2): the step's phases run in one cooperative launch, separated by
+// grid-wide barriers.  A phase is one GEMV, the attention chunks, their merge, or the output rows.
+// ---------------------------------------------------------------------------------------------
+enum PhaseType : int { PH_GEMV = 0, PH_ATTN = 1, PH_MERGE = 2, PH_FINAL = 3 };
+// The step's input and output pointers are kernel arguments, not part of the phase list, so one
+// list (and one captured graph) serves every input/output buffer pair.
+enum StepIo : int { IO_X = 1, IO_RES = 2, IO_OUT = 4 };  // g.x, g.res := x_in; f.out := out
+
+struct StepPhase {
+    int type;              // PhaseType
+    int nj;                // PH_GEMV: 16-byte weight granules per lane (1..4)
+    int stage_attn;        // index of a later PH_ATTN phase whose K/V chunk each CTA starts
+                           // staging into shared memory when this phase begins (-1: none)
+    int io;                // StepIo bits: fields that take the launch's input / output pointer
+    const float* stage_kc; // stage_attn >= 0: that phase's K and V caches
+    const float* stage_vc;
+    GemvParams g;          // PH_GEMV
+    AttnParams a;          // PH_ATTN, PH_MERGE
+    FinalParams f;         // PH_FINAL
+};
+
+// Grid barrier of the persistent kernel: `count` only grows (mod 2^32), by one per CTA and
+// barrier; barrier k of a launch completes when count reaches base + (k + 1) * grid.  `base` is
+// the count at the start of a launch, written by CTA 0 after the launch's last barrier.  Both
+// start at zero (and are zeroed again after a wait gave up).
+struct GridBarrier {
+    unsigned count;
+    unsigned base;
+};
+
+struct StepParams {
+    const StepPhase* phases;  // device array
+    int n_phases;
+    int attn0;                // index of the first PH_ATTN phase (-1: none)
+    const float* x_in;        // the step's input rows [m][hidden]
+    float* out;               // the step's output rows [m][hidden]
+    GridBarrier* bar;
+    unsigned* status;
+};
+
+// CTAs of the persistent kernel on this device for the given weight dtype, rows and head_dim
+// (2 per SM when they fit, else 1; 0 when a cooperative launch is not possible).
+int step_grid(int dtype, int m, int d, int num_sms);
+cudaError_t step_configure();
+// One step: a cooperative launch of `grid` CTAs (grid = step_grid(...)).
+cudaError_t launch_step(const StepParams& sp, int dtype, int m, int d, int grid, cudaStream_t s);
 
 struct PrefillParams {
     int layers, n, G, d, slots, streams, stream;

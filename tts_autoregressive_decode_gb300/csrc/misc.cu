@@ -1,33 +1,19 @@
 // misc.cu -- the step's last kernel and the state-management kernels (sm_103a).
 #include "common.cuh"
+#include "final_row.cuh"
 #include "kernels.h"
 
 namespace dec {
 
-// Talker: out = x / sqrt(mean(x^2) + eps) * w (the final RMSNorm, RMSNORM_SRC); codec: the
-// residual stream is the output (Pocket TTS on wgpu: the codec transformer has no final norm).
-// One CTA per stream; it also advances that stream's length, which no other kernel of the step
-// reads after this one has passed griddepcontrol.wait.
+// The step's last kernel: the output row of each stream (final_row.cuh), one CTA per stream.  It
+// also advances that stream's length, which no other kernel of the step reads after this one has
+// passed griddepcontrol.wait.
 __global__ void __launch_bounds__(256) k_final(const FinalParams p) {
     __shared__ float red[8];
     const int r = blockIdx.x, tid = threadIdx.x;
     pdl_trigger();
     pdl_wait();
-    const float* x = p.x + (size_t)r * p.h;
-    float* out = p.out + (size_t)r * p.h;
-    if (p.w) {
-        float ss = 0.f;
-        for (int i = tid; i < p.h; i += 256) ss += x[i] * x[i];
-        ss = warp_sum(ss);
-        if ((tid & 31) == 0) red[tid >> 5] = ss;
-        __syncthreads();
-        float tot = 0.f;
-        for (int w = 0; w < 8; ++w) tot += red[w];
-        const float inv = 1.0f / sqrtf(tot / (float)p.h + p.eps);
-        for (int i = tid; i < p.h; i += 256) out[i] = x[i] * inv * p.w[i];
-    } else {
-        for (int i = tid; i < p.h; i += 256) out[i] = x[i];
-    }
+    final_row(p, r, red);
     if (tid == 0) p.len[r] += 1;
 }
 
