@@ -46,7 +46,7 @@ NCU_TRAFFIC = {
     # gate/up GEMV (k_gemv_rows<bf16, m1, NJ1>, N = 12288, K = 2048): one launch captured with
     # ncu --set full on the 2-layer case of the same shapes (profiles/k_gemv_rows_gateup_*.md);
     # a launch does the same work at any layer count
-    W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_381_312, "source_sha": "3bdd5a5d53c5516a"},
+    W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_381_312, "source_sha": "df48366137bc5e9d"},
 }
 
 
@@ -106,15 +106,18 @@ def dominant_kernel(w: W.Workload, m: int):
     return (3, "LayerNorm + lin1 GEMV + GELU (k_gemv)", I * h * es + 4 * (m * h + 2 * h + m * I))
 
 
-def kernel_source_sha() -> str:
-    """Hash of every kernel source file: a stored ncu traffic figure is only reported for the
-    sources it was measured on."""
+# the sources the gate/up GEMV (k_gemv_rows) is compiled from
+GEMV_SOURCES = ("gemv.cu", "gemv_rows.cuh", "common.cuh", "kernels.h")
+
+
+def kernel_source_sha(files=GEMV_SOURCES) -> str:
+    """Hash of the dominant kernel's source files: a stored ncu traffic figure is only reported
+    for the sources it was measured on."""
     d = os.path.join(ROOT, "tts_autoregressive_decode_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(d, f), "rb").read())
+    for f in files:
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 

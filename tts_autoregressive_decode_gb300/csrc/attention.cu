@@ -32,16 +32,14 @@ size_t attention_ml_bytes(int m, int H, int max_chunks) {
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) {
-    constexpr int CH = kAttnChunk;
     extern __shared__ __align__(128) float smem[];
     const ChunkSmem sm = chunk_smem<D>(smem);
     float* const Ks = sm.Ks;
-    float* const s_l = sm.s_l;
     __shared__ __align__(8) uint64_t bar;
     __shared__ int s_last;
 
     const int c = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int group = p.H / p.G;
 
     const ChunkInfo ci = chunk_info(p, r, c);
@@ -64,7 +62,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) 
     pdl_wait();
     if (!chunk_compute<D>(p, r, g, c, ci, sm, bar_a, 0)) return;
 
-    // with no ticket array the partials are merged by the separate merge kernel
+    // with no ticket array the partials are merged by k_attn_merge
     if (nch == 1 || !p.tickets) return;
 
     // ---- ticket: the last CTA of (r, g) merges the chunks ---------------------------------------
@@ -78,82 +76,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) 
     if (!s_last) return;
     __threadfence();
 
-    // Stage every chunk's (m, l) of the group's heads in shared memory with independent loads
-    // (the K/V tiles are no longer needed), then the per-head max M, denominator and chunk
-    // weights w_c = exp(m_c - M); chunks without a legal key (l == 0) weigh 0.
-    float* wsc = Ks;                               // [group][nch] chunk weights
-    float* buf = Ks + kMaxGroup * ((p.max_chunks + 3) & ~3);  // partial outputs, batched
-    for (int idx = tid; idx < group * nch; idx += kAttnThreads) {
-        const int i = idx / nch, cc = idx - i * nch;
-        const size_t pi = ((size_t)r * p.H + g * group + i) * p.max_chunks + cc;
-        const float mc = __ldcg(p.part_ml + 2 * pi), lc = __ldcg(p.part_ml + 2 * pi + 1);
-        wsc[i * nch + cc] = lc > 0.f ? mc : -CUDART_INF_F;
-        buf[idx] = lc;
-    }
-    __syncthreads();
-    for (int i = warp; i < group; i += kAttnWarps) {
-        float M = -CUDART_INF_F;
-        for (int cc = lane; cc < nch; cc += 32) M = fmaxf(M, wsc[i * nch + cc]);
-        M = warp_max(M);
-        float den = 0.f;
-        for (int cc = lane; cc < nch; cc += 32) {
-            const float mc = wsc[i * nch + cc];
-            const float wc = (mc == -CUDART_INF_F) ? 0.f : expf(mc - M);
-            wsc[i * nch + cc] = wc;
-            den += wc * buf[i * nch + cc];
-        }
-        den = warp_sum(den);
-        if (lane == 0) s_l[i] = den;
-    }
-    __syncthreads();
-    // out = sum_c w_c o_c / den, the partial rows fetched in batches of whole chunks
-    const int per_batch = (int)((2 * CH * D - kMaxGroup * ((p.max_chunks + 3) & ~3)) / (group * D));
-    float num[(kMaxGroup * D + kAttnThreads - 1) / kAttnThreads];
-#pragma unroll
-    for (int q = 0; q < (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads; ++q) num[q] = 0.f;
-    for (int c0 = 0; c0 < nch; c0 += per_batch) {
-        const int nb = min(per_batch, nch - c0);
-        const int total = nb * group * D;
-        constexpr int UNR = 16;  // independent loads in flight per thread
-        for (int base = 0; base < total; base += kAttnThreads * UNR) {
-            float tmp[UNR];
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                const int idx = base + u * kAttnThreads + tid;
-                tmp[u] = 0.f;
-                if (idx < total) {
-                    const int cc = idx / (group * D), rem = idx - cc * group * D;
-                    const int i = rem / D, t = rem - i * D;
-                    const size_t pi = ((size_t)r * p.H + g * group + i) * p.max_chunks + c0 + cc;
-                    tmp[u] = __ldcg(p.part + pi * D + t);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                const int idx = base + u * kAttnThreads + tid;
-                if (idx < total) buf[idx] = tmp[u];
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads; ++q) {
-            const int o = tid + q * kAttnThreads;
-            if (o < group * D) {
-                const int i = o / D;
-                for (int cc = 0; cc < nb; ++cc)
-                    num[q] += wsc[i * nch + c0 + cc] * buf[cc * group * D + o];
-            }
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int q = 0; q < (kMaxGroup * D + kAttnThreads - 1) / kAttnThreads; ++q) {
-        const int o = tid + q * kAttnThreads;
-        if (o < group * D) {
-            const int i = o / D, t = o - i * D;
-            p.out[((size_t)r * p.H + g * group + i) * D + t] = num[q] / s_l[i];
-        }
-    }
+    // merge the group's q heads (items r H + g group + i), kAttnThreads / D at a time; the K/V
+    // tiles are no longer needed, so their area is the scratch
+    for (int i0 = 0; i0 < group; i0 += kAttnThreads / D)
+        merge_items<D, kAttnThreads>(p, r * p.H + g * group + i0, r * p.H + (g + 1) * group, Ks);
     if (tid == 0) p.tickets[r * p.G + g] = 0u;
 }
 
@@ -183,7 +109,7 @@ __global__ void __launch_bounds__(D) k_attn_merge(const AttnParams p) {
     __shared__ float scratch[2 * (kMaxSlots / kAttnChunk)];
     pdl_trigger();
     pdl_wait();
-    merge_items<D, D>(p, blockIdx.y * p.H + blockIdx.x, scratch);
+    merge_items<D, D>(p, blockIdx.y * p.H + blockIdx.x, p.m * p.H, scratch);
 }
 
 template <int D>

@@ -393,7 +393,7 @@ __device__ bool chunk_compute(const AttnParams& p, int r, int g, int c, const Ch
 }
 
 // Merge of the chunk partials of NT / D (q head, stream) items at once, D threads per item:
-// items item0 .. item0 + NT/D - 1 of the list r * H + hq.  Thread t of an item owns output
+// items item0 .. min(item0 + NT/D, item_end) - 1 of the list r * H + hq.  Thread t of an item owns output
 // dimension t and sums the chunks in ascending order.  The chunk statistics and the first
 // kMergeFirst partial values are fetched in one round of independent loads.  `scratch` holds
 // 2 * max_chunks floats per item.  All NT threads call it (block-wide barriers inside).
@@ -401,12 +401,12 @@ constexpr int kMergeFirst = 48;  // partial rows of the first round (covers 3072
 constexpr int kMergeBatch = 16;  // partial rows per later round
 
 template <int D, int NT>
-__device__ void merge_items(const AttnParams& p, int item0, float* scratch) {
+__device__ void merge_items(const AttnParams& p, int item0, int item_end, float* scratch) {
     constexpr int CH = kAttnChunk;
     const int sub = threadIdx.x / D, t = threadIdx.x - sub * D;
     const int item = item0 + sub;
     int nch = 0, r = 0, hq = 0;
-    if (item < p.m * p.H) {
+    if (item < item_end) {
         r = item / p.H;
         hq = item - r * p.H;
         const int len = __ldcg(p.len + r);

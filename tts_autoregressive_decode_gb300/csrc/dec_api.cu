@@ -274,7 +274,7 @@ bool stage_params(dec_ctx* ctx, int l, int stage, int m, const float* x_in, Gemv
             a.max_pos = c.max_pos;
             a.part = ctx->part;
             a.part_ml = ctx->part_ml;
-            a.tickets = nullptr;  // partials are merged by the merge kernel / phase
+            a.tickets = nullptr;  // the partials are merged by k_attn_merge (or a merge phase)
             a.max_chunks = ctx->max_chunks;
             a.out = ctx->attn;
             a.status = ctx->status;

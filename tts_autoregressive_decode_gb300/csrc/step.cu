@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                 constexpr int SUB = kStepThreads / D;
                 const int total = cur.a.m * cur.a.H;
                 for (int base_item = b * SUB; base_item < total; base_item += P * SUB)
-                    merge_items<D, kStepThreads>(cur.a, base_item, dsm);
+                    merge_items<D, kStepThreads>(cur.a, base_item, total, dsm);
                 break;
             }
             default:  // PH_FINAL
