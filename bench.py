@@ -61,6 +61,8 @@ def parse():
     p.add_argument("--layers", type=int, default=0,
                    help="keep only the first N layers (small cases for profiler captures)")
     p.add_argument("--kernel-rounds", type=int, default=20)
+    p.add_argument("--prefill-rows", type=int, default=64,
+                   help="rows of the timed prefill block (talker workloads; 0: skip)")
     p.add_argument("--plan", choices=["kernels", "persistent"], default="kernels",
                    help="step plan: the chain of kernels (default) or the persistent kernel")
     p.add_argument("--no-e2e", action="store_true")
@@ -379,6 +381,33 @@ def run_ours(args):
     tr = NCU_TRAFFIC.get(w.name)
     traffic = tr["bytes_per_launch"] if tr and tr.get("source_sha") == sha else None
 
+    # ---- batched causal prefill (talker): a 64-row block at the workload's first position -------
+    prefill = None
+    if talker and args.prefill_rows > 0 and base[0] + args.prefill_rows <= syn.max_pos:
+        n = args.prefill_rows
+        xp = torch.randn((n, h), generator=torch.Generator().manual_seed(7)).cuda()
+        yp = torch.empty_like(xp)
+        times = []
+        for rep in range(4):
+            dec.truncate(0, base[0])
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dec.prefill(0, xp, yp)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if rep:
+                times.append(a.elapsed_time(b))
+        dec.truncate(0, base[0])
+        pms = statistics.median(times)
+        rows = dec.prefill_rows()
+        blocks = (n + rows - 1) // rows
+        pbytes = blocks * (w.matrix_bytes() + vector_bytes(w)) + kv_bytes(w, [base[0] + i for i in range(n)])
+        prefill = {"rows": n, "block_rows": rows, "ms": pms, "tokens_per_s": n / (pms * 1e-3),
+                   "achieved_hbm_gbs": pbytes / (pms * 1e-3) / 1e9,
+                   "bytes": pbytes, "position": base[0],
+                   "note": "weights read once per block of block_rows rows"}
+
     # ---- end to end through the C ABI with host buffers ----------------------------------------
     e2e = None
     if not args.no_e2e:
@@ -442,7 +471,7 @@ def run_ours(args):
         "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                           "frac": step_gbs / peak, "bytes_per_step": nb},
         "gpu_launches": launches,
-        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "prefill": prefill,
     }
     print(json.dumps(line))
     if pg:

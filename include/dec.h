@@ -142,6 +142,23 @@ dec_status dec_set_stream(dec_ctx* ctx, void* stream);
  * (n_pos > max_pos for the talker, n_pos > ring for the codec). */
 dec_status dec_prefill_kv(dec_ctx* ctx, int stream, const float* k, const float* v, int n_pos);
 
+/* Batched causal prefill (Qwen3-TTS talker on wgpu, prefill() / forward_rows()): append the n
+ * rows of x to stream `stream` at positions len .. len + n - 1 and return every position's
+ * final-norm hidden.  Row r attends to keys 0 .. len + r: the block's own K/V rows are appended
+ * before its attention, so the block is causal within itself, and the result equals n single
+ * steps up to the order of floating-point sums.  Talker only.
+ *   x    DEVICE [n][hidden] f32 (16-byte aligned)
+ *   out  DEVICE [n][hidden] f32, must not overlap x
+ * Asynchronous on the context's stream; runs in blocks of up to 8 rows (each weight matrix is
+ * read once per block), launched directly (no graph).  The stream's length advances by n.
+ * Errors: DEC_E_ARG (stream, n < 1, NULL), DEC_E_UNSUPPORTED (codec: a KV ring takes one position
+ * per step), DEC_E_CAPACITY (len + n > max_pos); the state is unchanged on these. */
+dec_status dec_prefill(dec_ctx* ctx, int stream, int n, const float* x, float* out);
+
+/* Rows per dec_prefill block (each block reads every weight matrix once); 0 when the context
+ * does not serve prefill (codec) or ctx is NULL. */
+int dec_prefill_block_rows(const dec_ctx* ctx);
+
 /* One decode step of streams 0..m-1 (Qwen3-TTS talker on wgpu, step(): the new K/V row is
  * appended at `pos`, attention covers pos + 1 keys, the final-norm hidden is returned;
  * Pocket TTS on wgpu, step_device(): the output stays on the device).

@@ -69,6 +69,7 @@ def lib(precision: str = "f32") -> C.CDLL:
         L.orc_create.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcLayer), _fp]
         L.orc_prefill_kv.argtypes = [C.c_void_p, C.c_int, _fp, _fp, C.c_int]
         L.orc_step.argtypes = [C.c_void_p, C.c_int, _fp, C.POINTER(C.c_int), _dp, _dp]
+        L.orc_prefill.argtypes = [C.c_void_p, C.c_int, C.c_int, _fp, _dp]
         L.orc_reset.argtypes = [C.c_void_p, C.c_int]
         L.orc_len.argtypes = [C.c_void_p, C.c_int]
         L.orc_read_kv.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, _dp, _dp]
@@ -265,6 +266,17 @@ class OracleModel:
         if rc != 0:
             raise ValueError(f"orc_step failed ({rc})")
         return (out, t) if taps else out
+
+    def prefill(self, stream: int, x_in: np.ndarray) -> np.ndarray:
+        """Causal prefill of the rows of x_in [n][hidden] into `stream`: every position's
+        final-norm hidden [n][hidden]."""
+        x_in = np.ascontiguousarray(x_in, dtype=np.float32)
+        n = x_in.shape[0]
+        out = np.empty((n, self.w.hidden), np.float64)
+        rc = self.L.orc_prefill(self.h, stream, n, _ptr(x_in, C.c_float), _ptr(out, C.c_double))
+        if rc != 0:
+            raise ValueError(f"orc_prefill failed ({rc})")
+        return out
 
     def length(self, stream: int) -> int:
         return int(self.L.orc_len(self.h, stream))

@@ -599,3 +599,28 @@ int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* 
     free(y);
     return 0;
 }
+
+int orc_prefill(orc_model* m, int stream, int n, const float* x_in, double* out) {
+    if (!m || stream < 0 || stream >= m->c.streams || n < 1 || !x_in || !out) return -1;
+    const orc_config* c = &m->c;
+    if (c->kind != ORC_TALKER) return -4;
+    if (m->len[stream] + n > c->max_pos) return -3;
+    const int h = c->hidden;
+    size_t nbuf = (size_t)8 * h + 4 * (size_t)c->q_heads * c->head_dim +
+                  4 * (size_t)c->inter + (size_t)c->head_dim + 2 * (size_t)m->slots + 64;
+    real* buf = (real*)malloc(sizeof(real) * nbuf);
+    real* x = (real*)malloc(sizeof(real) * (size_t)h);
+    real* y = (real*)malloc(sizeof(real) * (size_t)h);
+    for (int r = 0; r < n; ++r) {  /* row r: one step at position len + r */
+        const int pos = m->len[stream];
+        for (int i = 0; i < h; ++i) x[i] = (real)x_in[(size_t)r * h + i];
+        for (int l = 0; l < c->layers; ++l) talker_layer(m, l, stream, pos, x, buf);
+        rms_norm_r(x, m->final_norm, h, (real)c->norm_eps, y);
+        from_real(y, h, out + (size_t)r * h);
+        m->len[stream] += 1;
+    }
+    free(buf);
+    free(x);
+    free(y);
+    return 0;
+}

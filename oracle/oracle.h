@@ -110,6 +110,14 @@ int orc_prefill_kv(orc_model* m, int stream, const float* k, const float* v, int
  * x_in [rows][hidden] f32; out [rows][hidden]; taps (nullable) [layers][rows][hidden] =
  * the residual stream after each layer.  Returns 0 or a negative error code. */
 int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* out, double* taps);
+
+/* Causal prefill of n rows of one stream (Qwen3-TTS talker on wgpu, prefill(): the block is
+ * appended at positions len .. len+n-1 and every position's final-norm hidden is returned).
+ * Its plain definition is the autoregressive one: row r is one talker step of `stream` at
+ * position len + r, which attends to keys 0 .. len + r -- exactly the keys a batched block with
+ * a causal mask gives row r.  x_in [n][hidden], out [n][hidden].  Talker only.
+ * Returns 0, or < 0 on a bad argument or capacity. */
+int orc_prefill(orc_model* m, int stream, int n, const float* x_in, double* out);
 void orc_reset(orc_model* m, int stream);
 int orc_len(const orc_model* m, int stream);
 /* read the stored key/value of (layer, stream, position) as [kv_heads][head_dim] */

@@ -362,6 +362,25 @@ def _talker_by_primitives(syn, x_in, pos, kv):
     return _f32(oracle.rms_norm(x, syn.final_norm, w.norm_eps))
 
 
+def test_prefill_is_causal_steps_of_pinned_primitives():
+    """A prefill block of n rows: row r is the page-order step at position len + r, attending to
+    every earlier key including the block's own earlier rows (causal within the block)."""
+    w = W.TALKER_H256_L1
+    syn = W.generate(w)
+    syn.max_pos = 40
+    m = oracle.OracleModel(syn)
+    x = np.random.default_rng(5).standard_normal((4, w.hidden)).astype(np.float32)
+    got = m.prefill(0, x)
+    kv = [([syn.prefill_k[0][l, p] for p in range(32)], [syn.prefill_v[0][l, p] for p in range(32)])
+          for l in range(w.layers)]
+    for r in range(4):
+        want = _talker_by_primitives(syn, x[r], 32 + r, kv)
+        assert np.array_equal(got[r], want.astype(np.float64)), r
+    assert m.length(0) == 36
+    with pytest.raises(ValueError):  # 36 + 5 > max_pos
+        m.prefill(0, np.zeros((5, w.hidden), np.float32))
+
+
 def test_talker_step_is_the_page_order_of_pinned_primitives():
     w = W.TALKER_H256_L1
     syn = W.generate(w)

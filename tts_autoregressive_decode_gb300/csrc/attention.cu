@@ -133,6 +133,53 @@ cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl
     return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Prefill block append: one warp per (row r, kv head g) computes the talker's new key (k-norm,
+// rope at len[stream] + r) and value, as the step's attention prologue does, and writes them to
+// the cache of p.stream.  The attention of the block runs after it, so every row sees the keys
+// of the rows before it (causal within the block).
+// ---------------------------------------------------------------------------------------------
+constexpr int kAppendWarps = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32) k_prefill_append(const AttnParams p) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int idx = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+    if (idx >= p.m * p.G) return;
+    const int r = idx / p.G, g = idx - r * p.G;
+    const int base = __ldcg(p.len + p.stream);
+    const int pos = base + r;
+    if (base < 0 || pos >= p.max_pos || pos >= p.slots) {
+        if (lane == 0) flag_check(p.status, CHECK_BOUNDS);
+        return;
+    }
+    const size_t row = (((size_t)p.stream * p.G + g) * p.slots + pos) * D;
+    talker_new_kv<D>(p, r, g, pos, lane, p.kc + row, p.vc + row);
+}
+
+template <int D>
+static cudaError_t launch_append_t(const AttnParams& p, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.m * p.G + kAppendWarps - 1) / kAppendWarps);
+    cfg.blockDim = dim3(kAppendWarps * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_prefill_append<D>, p);
+}
+
+cudaError_t launch_prefill_append(const AttnParams& p, cudaStream_t s, bool pdl) {
+    if (p.mode != ATTN_PREFILL) return cudaErrorInvalidValue;
+    if (p.d == 64) return launch_append_t<64>(p, s, pdl);
+    if (p.d == 128) return launch_append_t<128>(p, s, pdl);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t attention_configure() {
     cudaError_t e = cudaFuncSetAttribute(k_attention<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)attention_smem_bytes(64, kMaxGroup));

@@ -98,7 +98,13 @@ __device__ __forceinline__ ChunkSmem chunk_smem(float* base) {
     return s;
 }
 
-// Which keys chunk c of stream r covers, and whether the stream's position is usable.
+// The stream whose cache row r of a launch reads: the row itself, or for a prefill block the
+// block's stream.
+__device__ __forceinline__ int cache_stream(const AttnParams& p, int r) {
+    return p.mode == ATTN_PREFILL ? p.stream : r;
+}
+
+// Which keys chunk c of row r covers, and whether the row's position is usable.
 struct ChunkInfo {
     int pos;      // TALKER/RING: the step's position
     int nch;      // chunks of the stream
@@ -115,12 +121,21 @@ __device__ __forceinline__ ChunkInfo chunk_info(const AttnParams& p, int r, int 
     ci.pos = 0;
     ci.k0 = c * CH;
     ci.newrow = -1;
-    const int len = __ldcg(p.len + r);
+    const int len = p.mode == ATTN_PREFILL ? 0 : __ldcg(p.len + r);
     if (p.mode == ATTN_PLAIN) {
         ci.nch = (len + CH - 1) / CH;
         ci.nk = min(CH, len - ci.k0);
         ci.ncached = ci.nk;
         ci.bad = ci.nch > p.max_chunks || len > p.slots || len < 1;
+    } else if (p.mode == ATTN_PREFILL) {
+        const int base = __ldcg(p.len + p.stream);  // the stream's length before the block
+        ci.pos = base + r;
+        const int L = ci.pos + 1;
+        ci.nch = (L + CH - 1) / CH;
+        ci.nk = min(CH, L - ci.k0);
+        ci.ncached = ci.nk;  // the block's own rows are already in the cache
+        ci.bad = base < 0 || ci.pos >= p.max_pos || ci.pos >= p.slots;
+        (void)len;
     } else if (p.mode == ATTN_TALKER) {
         ci.pos = len;
         const int L = len + 1;
@@ -146,7 +161,7 @@ __device__ __forceinline__ ChunkInfo chunk_info(const AttnParams& p, int r, int 
 template <int D>
 __device__ __forceinline__ void chunk_issue(const AttnParams& p, int r, int g, const ChunkInfo& ci,
                                             const ChunkSmem& sm, uint32_t bar) {
-    const size_t head_base = ((size_t)r * p.G + g) * p.slots;
+    const size_t head_base = ((size_t)cache_stream(p, r) * p.G + g) * p.slots;
     const uint32_t bytes = (uint32_t)(ci.ncached > 0 ? ci.ncached : 0) * D * sizeof(float);
     mbar_arrive_expect_tx(bar, 2 * bytes);
     if (bytes) {
@@ -178,6 +193,39 @@ __device__ __forceinline__ float butterfly8_keys(const float v[8], int lane) {
     return c;
 }
 
+// The talker's new key and value of kv head g from raw q/k/v row `row` (per-head RMSNorm of k
+// with the shared [d] weight, rotate_half rope at `pos`; v as is), by one warp: element
+// t = lane + 32 j of the results is written to k_out[t] and v_out[t].
+template <int D>
+__device__ __forceinline__ void talker_new_kv(const AttnParams& p, int row, int g, int pos,
+                                              int lane, float* k_out, float* v_out) {
+    constexpr int HALF = D / 2;
+    const float* ksrc = p.qkv + (size_t)row * p.ldqkv + (size_t)p.H * D + (size_t)g * D;
+    const float* vsrc = ksrc + (size_t)p.G * D;
+    float v[D / 32];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+        v[j] = __ldcg(ksrc + lane + 32 * j);
+        ss += v[j] * v[j];
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)D + p.eps);
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) v[j] = v[j] * inv * p.kn[lane + 32 * j];
+    const float* cs = p.rope_cos + (size_t)pos * HALF;
+    const float* sn = p.rope_sin + (size_t)pos * HALF;
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+        const int t = lane + 32 * j;
+        const int jj = (j + D / 64) % (D / 32);  // element t +- D/2, same lane
+        const float rot = (t < HALF) ? -v[jj] : v[jj];
+        const int f = t < HALF ? t : t - HALF;
+        k_out[t] = v[j] * cs[f] + rot * sn[f];
+        v_out[t] = __ldcg(vsrc + t);
+    }
+}
+
 // The item's work once its copies were issued with chunk_issue (barrier phase `parity`): the
 // prologue, the wait for the staged rows, the append, scores, the chunk softmax statistics and
 // the partial (or, for a single-chunk stream, the final output).  The NT threads of a group call
@@ -207,7 +255,7 @@ __device__ bool chunk_compute(const AttnParams& p, int r, int g, int c, const Ch
         if (mode == ATTN_PLAIN) {
             for (int t = lane; t < D; t += 32)
                 qs[i * D + t] = __ldcg(p.qkv + ((size_t)r * p.H + hq) * D + t);
-        } else if (mode == ATTN_TALKER) {
+        } else if (mode == ATTN_TALKER || mode == ATTN_PREFILL) {
             const float* src = p.qkv + (size_t)r * p.ldqkv + (size_t)hq * D;
             float v[D / 32];
             float ss = 0.f;
@@ -244,30 +292,7 @@ __device__ bool chunk_compute(const AttnParams& p, int r, int g, int c, const Ch
     if (newrow >= 0 && warp == (group % kChunkWarps)) {
         // the new key and value of kv head g at position pos
         if (mode == ATTN_TALKER) {
-            const float* ksrc = p.qkv + (size_t)r * p.ldqkv + (size_t)p.H * D + (size_t)g * D;
-            const float* vsrc = ksrc + (size_t)p.G * D;
-            float v[D / 32];
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < D / 32; ++j) {
-                v[j] = __ldcg(ksrc + lane + 32 * j);
-                ss += v[j] * v[j];
-            }
-            ss = warp_sum(ss);
-            const float inv = 1.0f / sqrtf(ss / (float)D + p.eps);
-#pragma unroll
-            for (int j = 0; j < D / 32; ++j) v[j] = v[j] * inv * p.kn[lane + 32 * j];
-            const float* cs = p.rope_cos + (size_t)pos * HALF;
-            const float* sn = p.rope_sin + (size_t)pos * HALF;
-#pragma unroll
-            for (int j = 0; j < D / 32; ++j) {
-                const int t = lane + 32 * j;
-                const int jj = (j + D / 64) % (D / 32);
-                const float rot = (t < HALF) ? -v[jj] : v[jj];
-                const int f = t < HALF ? t : t - HALF;
-                sm.knew[t] = v[j] * cs[f] + rot * sn[f];
-                sm.vnew[t] = __ldcg(vsrc + t);
-            }
+            talker_new_kv<D>(p, r, g, pos, lane, sm.knew, sm.vnew);
         } else {
             const int D_model = p.H * D;
             const float* ksrc = p.qkv + (size_t)r * p.ldqkv + D_model + (size_t)g * D;
@@ -295,7 +320,7 @@ __device__ bool chunk_compute(const AttnParams& p, int r, int g, int c, const Ch
         return false;
     }
     if (newrow >= 0) {
-        const size_t head_base = ((size_t)r * p.G + g) * p.slots;
+        const size_t head_base = ((size_t)cache_stream(p, r) * p.G + g) * p.slots;
         for (int t = tid; t < D; t += NT) {
             Ks[newrow * D + t] = sm.knew[t];
             Vs[newrow * D + t] = sm.vnew[t];
@@ -409,10 +434,10 @@ __device__ void merge_items(const AttnParams& p, int item0, int item_end, float*
     if (item < item_end) {
         r = item / p.H;
         hq = item - r * p.H;
-        const int len = __ldcg(p.len + r);
         int L;
-        if (p.mode == ATTN_PLAIN) L = len;
-        else L = (p.mode == ATTN_TALKER) ? len + 1 : p.slots;
+        if (p.mode == ATTN_PREFILL) L = __ldcg(p.len + p.stream) + r + 1;
+        else if (p.mode == ATTN_PLAIN) L = __ldcg(p.len + r);
+        else L = (p.mode == ATTN_TALKER) ? __ldcg(p.len + r) + 1 : p.slots;
         nch = (L + CH - 1) / CH;
         if (L < 1 || nch <= 1 || nch > p.max_chunks) nch = 0;  // one chunk: already final
     }

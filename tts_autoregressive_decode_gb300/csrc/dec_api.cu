@@ -97,6 +97,8 @@ struct dec_ctx {
     cudaStream_t cap_stream = nullptr;
     int num_sms = 0;
     int S = 0;              // streams
+    int R = 0;              // rows of the activation scratch: max(S, prefill block rows)
+    int prefill_rows = 0;   // rows of a prefill block (0: prefill not served)
     int slots = 0;          // KV rows per (layer, stream, kv head)
     int qkv_rows = 0;       // rows of the fused q/k/v matrix
     int max_chunks = 0;     // attention chunks per (stream, kv head)
@@ -350,6 +352,7 @@ FinalParams final_params(dec_ctx* ctx, int m, float* out) {
     f.eps = c.norm_eps;
     f.out = out;
     f.len = ctx->len_dev;
+    f.advance_stream = -1;
     return f;
 }
 
@@ -420,6 +423,37 @@ StepParams step_params(dec_ctx* ctx, const StepPhase* phases, const float* x_in,
     sp.x_in = x_in;
     sp.out = out;
     return sp;
+}
+
+// Enqueue one prefill block of m rows of stream `stream` (Qwen3-TTS talker on wgpu,
+// forward_rows): the step's kernels with m rows of one stream, plus the append of the block's
+// K/V rows before its attention, which then runs in ATTN_PREFILL mode (row r sees keys up to
+// len + r).  The final kernel advances the stream by m.
+cudaError_t enqueue_prefill_block(dec_ctx* ctx, int stream, int m, const float* x_in, float* out,
+                                  cudaStream_t s) {
+    const dec_config& c = ctx->cfg;
+    cudaError_t e;
+    for (int l = 0; l < c.layers; ++l)
+        for (int stage = 0; stage < 5; ++stage) {
+            const bool pdl = l > 0 || stage > 0;
+            GemvParams g;
+            AttnParams a;
+            if (!stage_params(ctx, l, stage, m, x_in, g, a)) {
+                g.tap = nullptr;  // taps hold the last step's rows, not a block's
+                if ((e = launch_gemv(g, c.weight_dtype, ctx->num_sms, s, pdl)) != cudaSuccess) return e;
+                continue;
+            }
+            a.mode = ATTN_PREFILL;
+            a.stream = stream;
+            if ((e = launch_prefill_append(a, s, pdl)) != cudaSuccess) return e;
+            // not a programmatic dependent: the attention stages cache rows before its
+            // griddepcontrol.wait, and the append above writes this block's rows
+            if ((e = launch_attention(a, s, false)) != cudaSuccess) return e;
+            if ((e = launch_attention_merge(a, s, true)) != cudaSuccess) return e;
+        }
+    FinalParams f = final_params(ctx, m, out);
+    f.advance_stream = stream;
+    return launch_final(f, s, true);
 }
 
 // Enqueue one step of a plan: the persistent kernel when the plan has a phase list, else the
@@ -714,10 +748,17 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     const size_t o_pr = talker ? 0 : take((size_t)c.layers * S * ctx->slots * 4);
     const size_t half = d / 2;
     const size_t o_cos = take((size_t)c.max_pos * half * 4), o_sin = take((size_t)c.max_pos * half * 4);
-    const size_t o_x = take((size_t)S * h * 4), o_qkv = take((size_t)S * ctx->qkv_rows * 4);
-    const size_t o_att = take((size_t)S * qw * 4), o_act = take((size_t)S * I * 4);
-    const size_t o_part = take(attention_part_bytes(S, H, ctx->max_chunks, d));
-    const size_t o_ml = take(attention_ml_bytes(S, H, ctx->max_chunks));
+    // a prefill block takes up to 8 rows, as many as the m > 2 GEMV's shared-memory stage allows
+    if (talker) {
+        const int widest = std::max(std::max(h, I), qw);
+        for (int rows = 8; rows >= 1 && !ctx->prefill_rows; --rows)
+            if (gemv_smem_bytes(rows, widest) <= (size_t)kGemvMaxSmem) ctx->prefill_rows = rows;
+    }
+    const int R = ctx->R = std::max(S, ctx->prefill_rows);
+    const size_t o_x = take((size_t)R * h * 4), o_qkv = take((size_t)R * ctx->qkv_rows * 4);
+    const size_t o_att = take((size_t)R * qw * 4), o_act = take((size_t)R * I * 4);
+    const size_t o_part = take(attention_part_bytes(R, H, ctx->max_chunks, d));
+    const size_t o_ml = take(attention_ml_bytes(R, H, ctx->max_chunks));
     const size_t o_len = take((size_t)S * 4), o_st = take(4), o_gbar = take(sizeof(GridBarrier));
     const size_t o_taps = (c.flags & DEC_FLAG_TAPS) ? take((size_t)c.layers * S * h * 4) : 0;
     const size_t o_in = take((size_t)S * h * 4), o_out = take((size_t)S * h * 4);
@@ -823,6 +864,30 @@ dec_status dec_prefill_kv(dec_ctx* ctx, int stream, const float* k, const float*
     ctx->len_host[stream] = n_pos;
     return DEC_OK;
 }
+
+dec_status dec_prefill(dec_ctx* ctx, int stream, int n, const float* x, float* out) {
+    if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");
+    if (ctx->cfg.kind != DEC_QWEN3_TALKER || ctx->prefill_rows < 1)
+        return fail(ctx, DEC_E_UNSUPPORTED, "prefill blocks are a talker operation (a KV ring takes one position per step)");
+    if (stream < 0 || stream >= ctx->S)
+        return fail(ctx, DEC_E_ARG, "stream %d outside 0..%d", stream, ctx->S - 1);
+    if (n < 1 || !x || !out) return fail(ctx, DEC_E_ARG, "n < 1 or a NULL buffer");
+    if (!aligned16(x) || !aligned16(out)) return fail(ctx, DEC_E_ARG, "x and out must be 16-byte aligned");
+    if ((long long)ctx->len_host[stream] + n > ctx->cfg.max_pos)
+        return fail(ctx, DEC_E_CAPACITY, "stream %d: length %d + %d exceeds max_pos %d", stream,
+                    ctx->len_host[stream], n, ctx->cfg.max_pos);
+    const size_t h = (size_t)ctx->cfg.hidden;
+    for (int r0 = 0; r0 < n; r0 += ctx->prefill_rows) {
+        const int m = std::min(ctx->prefill_rows, n - r0);
+        CUDA_TRY(ctx, enqueue_prefill_block(ctx, stream, m, x + (size_t)r0 * h, out + (size_t)r0 * h,
+                                            ctx->stream),
+                 "prefill launch");
+    }
+    ctx->len_host[stream] += n;
+    return DEC_OK;
+}
+
+int dec_prefill_block_rows(const dec_ctx* ctx) { return ctx ? ctx->prefill_rows : 0; }
 
 dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, float* hidden_out) {
     if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");

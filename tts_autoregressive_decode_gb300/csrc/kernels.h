@@ -64,6 +64,9 @@ enum AttnMode : int {
     ATTN_TALKER = 1,  // raw qkv: per-head q/k RMSNorm, rotate_half rope, append K/V at pos
     ATTN_RING = 2,    // raw qkv: interleaved rope, push K/V into slot pos % ring, stamp it;
                       // keys legal by stamp and window
+    ATTN_PREFILL = 3, // a block of rows of ONE stream (`stream`) at positions len[stream] + r:
+                      // raw qkv, q as ATTN_TALKER, keys 0..len[stream] + r (the block's K/V
+                      // rows already appended by k_prefill_append); nothing appended here
 };
 
 constexpr int kAttnChunk = 64;   // keys per CTA
@@ -72,7 +75,8 @@ constexpr int kMaxSlots = 32768; // cache rows per (stream, kv head): bounds the
 
 struct AttnParams {
     int mode;
-    int m;                 // rows (streams)
+    int m;                 // rows (streams; ATTN_PREFILL: rows of the block)
+    int stream;            // ATTN_PREFILL: the stream whose cache and length the rows use
     int H, G, d;           // q heads, kv heads, head_dim
     int slots;             // cache rows per (stream, kv head): capacity or ring
     int window;            // ring: attention window
@@ -100,6 +104,9 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl);
 cudaError_t attention_configure();
 // Merge of k_attention's chunk partials (launch after k_attention with tickets == nullptr).
 cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl);
+// ATTN_PREFILL blocks: q/k norm of the block's keys, rope, append to the cache of p.stream at
+// positions len[stream] + r (r < p.m); launch before the attention.
+cudaError_t launch_prefill_append(const AttnParams& p, cudaStream_t s, bool pdl);
 size_t attention_smem_bytes(int d, int group);
 // scratch sizes (bytes) for the partials and tickets
 size_t attention_part_bytes(int m, int H, int max_chunks, int d);
@@ -114,7 +121,8 @@ struct FinalParams {
     const float* w;        // talker final norm [h]; null = copy (codec)
     float eps;
     float* out;            // [m][h]
-    int32_t* len;          // [m]: incremented
+    int32_t* len;          // [m]: incremented (row r advances stream r) ...
+    int advance_stream;    // ... unless >= 0: a prefill block, which advances this stream by m
 };
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
 

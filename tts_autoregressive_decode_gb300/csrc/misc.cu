@@ -14,7 +14,12 @@ __global__ void __launch_bounds__(256) k_final(const FinalParams p) {
     pdl_trigger();
     pdl_wait();
     final_row(p, r, red);
-    if (tid == 0) p.len[r] += 1;
+    if (tid == 0) {
+        if (p.advance_stream < 0)
+            p.len[r] += 1;
+        else if (r == 0)
+            p.len[p.advance_stream] += p.m;
+    }
 }
 
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl) {

@@ -99,6 +99,20 @@ class Decoder:
         L.check(self.lib.dec_prefill_kv(self.h, stream, _ptr(k), _ptr(v), n), self.h)
         self.sync()  # keep the sources alive until the copy has run
 
+    def prefill(self, stream: int, x: torch.Tensor, out: Optional[torch.Tensor] = None
+                ) -> torch.Tensor:
+        """Append the n rows of x [n][hidden] (device f32) to `stream` at its next positions and
+        return every position's final-norm hidden [n][hidden] (asynchronous)."""
+        n = int(x.shape[0])
+        if out is None:
+            out = torch.empty_like(x)
+        L.check(self.lib.dec_prefill(self.h, stream, n, _ptr(x), _ptr(out)), self.h)
+        return out
+
+    def prefill_rows(self) -> int:
+        """Rows per prefill block (0: prefill not served)."""
+        return int(self.lib.dec_prefill_block_rows(self.h))
+
     def step(self, x: torch.Tensor, pos: Sequence[int], out: Optional[torch.Tensor] = None
              ) -> torch.Tensor:
         m = int(x.shape[0])
