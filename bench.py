@@ -83,8 +83,9 @@ def peaks():
 
 def vector_bytes(w: W.Workload) -> int:
     h, d = w.hidden, w.head_dim
-    per = (2 * h + 2 * d) if w.kind == "talker" else 6 * h
-    return 4 * (w.layers * per + (h if w.kind == "talker" else 0))
+    per = (2 * h + 2 * d) if w.kind == "talker" else (6 if w.layer_scale else 4) * h
+    tail = h if w.kind == "talker" else (3 * h if w.head else 0)  # final norm / out_norm + EOS
+    return 4 * (w.layers * per + tail)
 
 
 def kv_bytes(w: W.Workload, positions) -> int:
@@ -273,7 +274,8 @@ def run_ours(args):
     syn = W.generate(w)
     if not talker:
         # the ring keeps positions growing: size the RoPE table for warm-up + timed + e2e steps
-        syn.max_pos = max(syn.max_pos, 2 * (args.warmup + args.steps) + 2 * w.steps + 8)
+        syn.max_pos = max(syn.max_pos,
+                          max(syn.lengths) + 2 * (args.warmup + args.steps) + 2 * w.steps + 8)
     from tts_autoregressive_decode_gb300 import _lib
     dec = Decoder.from_synthetic(syn, flags=_lib.DEC_FLAG_PERSISTENT if args.plan == "persistent" else 0)
     m, h = w.streams, w.hidden

@@ -98,7 +98,8 @@ typedef struct {
  *         down [h][inter]; in_norm [h], q_norm [d], k_norm [d], post_norm [h] (f32).
  * Codec:  in_proj [3*hidden][hidden] with rows [q | k | v], each head-major; out_proj
  *         [hidden][hidden]; lin1 [inter][hidden]; lin2 [hidden][inter]; ln1_w, ln1_b,
- *         ln2_w, ln2_b, ls1, ls2 [hidden] (f32).  Fields of the other kind are ignored.
+ *         ln2_w, ln2_b, ls1, ls2 [hidden] (f32); ls1 / ls2 may be NULL (no LayerScale, as in
+ *         the FlowLM backbone).  Fields of the other kind are ignored.
  */
 typedef struct {
     const void *q, *k, *v, *o, *gate, *up, *down;
@@ -109,7 +110,14 @@ typedef struct {
 
 typedef struct {
     const dec_layer_weights* layers; /* HOST array of `layers` entries */
-    const float* final_norm;         /* talker: DEVICE [h] f32; codec: ignored */
+    const float* final_norm;         /* talker: the final RMSNorm weight, DEVICE [h] f32.
+                                        codec: NULL (the output is the residual stream, as in
+                                        Mimi) or the FlowLM backbone's out_norm LayerNorm weight */
+    const float* final_norm_b;       /* codec with final_norm: out_norm bias, DEVICE [h] f32 */
+    const float* eos_w;              /* codec, optional: the EOS row, DEVICE [h] f32; each step
+                                        then computes eos_w . output (Pocket TTS on wgpu,
+                                        PocketBackboneGpu: out_eos) */
+    float eos_b;                     /* the EOS bias, added when the logits are read */
 } dec_weights;
 
 typedef struct dec_ctx dec_ctx;
@@ -205,6 +213,10 @@ dec_status dec_read_kv(dec_ctx* ctx, int layer, int stream, int position, float*
 /* With DEC_FLAG_TAPS: copy the residual stream after `layer` of the last step to HOST
  * [m][hidden] f32 (the pages' stage probes, Mimi on wgpu, debug_read()).  Synchronous. */
 dec_status dec_read_tap(dec_ctx* ctx, int layer, int m, float* dst_host);
+
+/* With eos_w: the EOS logits of the last step of streams 0..m-1, bias added, into HOST [m]
+ * (waits for the context's stream).  Errors: DEC_E_ARG, DEC_E_UNSUPPORTED (no EOS row). */
+dec_status dec_read_eos(dec_ctx* ctx, int m, float* dst_host);
 
 /* Number of CUDA kernels one step of m rows launches (for launch accounting): 6 * layers + 1,
  * or 1 when the persistent kernel serves the step (DEC_FLAG_PERSISTENT, m <= 2). */

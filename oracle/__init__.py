@@ -70,6 +70,9 @@ def lib(precision: str = "f32") -> C.CDLL:
         L.orc_prefill_kv.argtypes = [C.c_void_p, C.c_int, _fp, _fp, C.c_int]
         L.orc_step.argtypes = [C.c_void_p, C.c_int, _fp, C.POINTER(C.c_int), _dp, _dp]
         L.orc_prefill.argtypes = [C.c_void_p, C.c_int, C.c_int, _fp, _dp]
+        L.orc_set_head.argtypes = [C.c_void_p, _fp, _fp, _fp]
+        L.orc_eos.argtypes = [C.c_void_p, C.c_int]
+        L.orc_eos.restype = C.c_double
         L.orc_reset.argtypes = [C.c_void_p, C.c_int]
         L.orc_len.argtypes = [C.c_void_p, C.c_int]
         L.orc_read_kv.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, _dp, _dp]
@@ -243,6 +246,14 @@ class OracleModel:
         self.h = self.L.orc_create(C.byref(cfg), arr, fn)
         if not self.h:
             raise ValueError("oracle rejected the configuration")
+        self.eos_bias = 0.0
+        if getattr(syn, "head", None) is not None:
+            hd = {k: np.ascontiguousarray(v, dtype=np.float32) for k, v in syn.head.items()}
+            self._keep.extend(hd.values())
+            if self.L.orc_set_head(self.h, _ptr(hd["norm_w"], C.c_float),
+                                   _ptr(hd["norm_b"], C.c_float), _ptr(hd["eos_w"], C.c_float)):
+                raise ValueError("oracle rejected the head")
+            self.eos_bias = float(hd["eos_b"][0])
         for s, n in enumerate(syn.lengths):
             if n > 0:
                 self.prefill_kv(s, syn.prefill_k[s], syn.prefill_v[s])
@@ -277,6 +288,10 @@ class OracleModel:
         if rc != 0:
             raise ValueError(f"orc_prefill failed ({rc})")
         return out
+
+    def eos(self, stream: int) -> float:
+        """The last step's EOS logit of `stream`, bias included (codec head only)."""
+        return float(self.L.orc_eos(self.h, stream)) + self.eos_bias
 
     def length(self, stream: int) -> int:
         return int(self.L.orc_len(self.h, stream))

@@ -355,6 +355,8 @@ struct orc_model {
     orc_config c;
     orc_layer* layers;
     const float* final_norm;
+    const float *head_w, *head_b, *eos_w;  /* codec head (FlowLM): out_norm and the EOS row */
+    double* eos;    /* [streams] the last step's EOS logit (without its bias) */
     int slots;      /* KV rows per (layer, stream): max_pos (talker) or ring (codec) */
     real* kc;       /* [layers][streams][slots][kv_heads][head_dim], position- or slot-major */
     real* vc;
@@ -387,6 +389,7 @@ orc_model* orc_create(const orc_config* cfg, const orc_layer* layers, const floa
     m->kc = (real*)calloc(n, sizeof(real));
     m->vc = (real*)calloc(n, sizeof(real));
     m->len = (int*)calloc((size_t)cfg->streams, sizeof(int));
+    m->eos = (double*)calloc((size_t)cfg->streams, sizeof(double));
     if (cfg->kind == ORC_CODEC) {
         size_t np = (size_t)cfg->layers * cfg->streams * cfg->ring;
         m->pr = (uint32_t*)malloc(np * sizeof(uint32_t));
@@ -406,7 +409,20 @@ void orc_destroy(orc_model* m) {
     free(m->vc);
     free(m->pr);
     free(m->len);
+    free(m->eos);
     free(m);
+}
+
+int orc_set_head(orc_model* m, const float* norm_w, const float* norm_b, const float* eos_w) {
+    if (!m || m->c.kind != ORC_CODEC || !norm_w || !norm_b) return -1;
+    m->head_w = norm_w;
+    m->head_b = norm_b;
+    m->eos_w = eos_w;
+    return 0;
+}
+
+double orc_eos(const orc_model* m, int stream) {
+    return (m && stream >= 0 && stream < m->c.streams) ? m->eos[stream] : 0.0;
 }
 
 int orc_len(const orc_model* m, int stream) {
@@ -555,12 +571,13 @@ static void codec_layer(orc_model* m, int l, int s, int pos, real* x, real* buf)
     ring_attention_r(q, m->kc + kv_index(m, l, s, 0), m->vc + kv_index(m, l, s, 0), pr, ring,
                      c->window, (uint32_t)pos, H, d, att, sc, legal);
     matvec_r(W->out_proj, bf, D, D, att, o);
-    for (int i = 0; i < D; ++i) x[i] = x[i] + (real)W->ls1[i] * o[i];
+    /* LayerScale multiplies the branch; the FlowLM backbone has none (a scale of one) */
+    for (int i = 0; i < D; ++i) x[i] = x[i] + (W->ls1 ? (real)W->ls1[i] * o[i] : o[i]);
     layer_norm_r(x, W->ln2_w, W->ln2_b, D, eps, hb);
     matvec_r(W->lin1, bf, F, D, hb, f);
     for (int i = 0; i < F; ++i) f[i] = gelu_r(f[i]);
     matvec_r(W->lin2, bf, D, F, f, y);
-    for (int i = 0; i < D; ++i) x[i] = x[i] + (real)W->ls2[i] * y[i];
+    for (int i = 0; i < D; ++i) x[i] = x[i] + (W->ls2 ? (real)W->ls2[i] * y[i] : y[i]);
 }
 
 int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* out,
@@ -589,6 +606,15 @@ int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* 
         if (c->kind == ORC_TALKER) {
             rms_norm_r(x, m->final_norm, h, (real)c->norm_eps, y);
             from_real(y, h, out + (size_t)s * h);
+        } else if (m->head_w) {
+            /* FlowLM backbone: out_norm, then the EOS logit of the normalized row */
+            layer_norm_r(x, m->head_w, m->head_b, h, (real)c->norm_eps, y);
+            from_real(y, h, out + (size_t)s * h);
+            if (m->eos_w) {
+                real e = 0;
+                for (int i = 0; i < h; ++i) e += (real)m->eos_w[i] * y[i];
+                m->eos[s] = (double)e;
+            }
         } else {
             from_real(x, h, out + (size_t)s * h);
         }

@@ -111,6 +111,14 @@ int orc_prefill_kv(orc_model* m, int stream, const float* k, const float* v, int
  * the residual stream after each layer.  Returns 0 or a negative error code. */
 int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* out, double* taps);
 
+/* Codec only: the FlowLM backbone's head (Pocket TTS on wgpu, PocketBackboneGpu): after the
+ * stack, out = LayerNorm(x; norm_w, norm_b) is the step's output instead of x, and with eos_w
+ * the EOS logit eos_w . out (ascending sum; its bias is added by the caller, as the page does on
+ * read-back) is kept per stream for orc_eos.  A codec layer with ls1 / ls2 NULL has no
+ * LayerScale.  Returns 0, or -1 on a bad argument. */
+int orc_set_head(orc_model* m, const float* norm_w, const float* norm_b, const float* eos_w);
+double orc_eos(const orc_model* m, int stream);
+
 /* Causal prefill of n rows of one stream (Qwen3-TTS talker on wgpu, prefill(): the block is
  * appended at positions len .. len+n-1 and every position's final-norm hidden is returned).
  * Its plain definition is the autoregressive one: row r is one talker step of `stream` at

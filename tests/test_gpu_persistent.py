@@ -34,7 +34,8 @@ def _widths(S, n):
     return [1 + t % S for t in range(n)]
 
 
-@pytest.mark.parametrize("name", ["small_talker_f32", "small_talker_bf16", "small_codec"])
+@pytest.mark.parametrize("name", ["small_talker_f32", "small_talker_bf16", "small_codec",
+                                  "small_flowlm"])
 def test_persistent_equals_multikernel_bitwise(D, name):
     w = W.SMALL[name]
     syn = W.generate(w)

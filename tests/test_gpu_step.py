@@ -24,7 +24,7 @@ def D():
     return decoder
 
 
-def run_parity(D, w, steps=None, flags=0, taps=False, report=None):
+def run_parity(D, w, steps=None, flags=0, taps=False, report=None, eos=False):
     """Run `steps` steps on both sides (each side feeds back its own output when the workload
     says so) and check every row of every step.  Returns the stats."""
     syn = W.generate(w, steps=steps)
@@ -53,10 +53,14 @@ def run_parity(D, w, steps=None, flags=0, taps=False, report=None):
             want = orc.step(xo, pos)
         got = out.cpu().numpy()
         check_rows(got, want, bf16, st, f"{w.name} step {t}")
-        if w.kind == "codec":
+        if w.kind == "codec" and not w.head:
             # the codec output is input + O(0.01) LayerScale terms: check the change as well
             check_rows(got - xg, want - xo.astype(np.float64), bf16, st_delta,
                        f"{w.name} step {t} delta")
+        if eos:  # the FlowLM head's EOS logits, bias included
+            ge = dec.read_eos(m)
+            for s in range(m):
+                assert abs(float(ge[s]) - orc.eos(s)) <= 5e-4, (t, s, float(ge[s]), orc.eos(s))
         if taps:
             for l in range(w.layers):
                 check_rows(dec.read_tap(l, m), want_taps[l], bf16, None, f"{w.name} step {t} tap {l}")
@@ -96,6 +100,18 @@ def test_codec_d512_l8_600_steps_two_ring_wraps(D):
     k, v = dec.read_kv(7, 0, 599)
     ko, vo = orc.read_kv(7, 0, 599)
     assert np.max(np.abs(k.reshape(-1) - ko.reshape(-1))) < 1e-3
+
+
+def test_flowlm_d1024_l6_64_steps_with_eos(D):
+    rep = []
+    run_parity(D, W.FLOWLM_D1024_L6, report=rep, eos=True)
+    print(rep[-1])
+
+
+def test_small_flowlm_eos_every_step(D):
+    rep = []
+    run_parity(D, W.SMALL_FLOWLM, report=rep, eos=True)
+    print(rep[-1])
 
 
 def test_talker_h2048_l28_bf16_128_steps(D):

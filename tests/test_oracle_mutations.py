@@ -32,7 +32,8 @@ MUTATIONS = [
     ("window_off_by_one", "(pos - pj < (uint32_t)window)", "(pos - pj <= (uint32_t)window)"),
     ("ring_stamp_dropped", "pr[slot] = (uint32_t)pos;", "(void)pr;"),
     ("talker_residual_dropped", "x[i] = x[i] + o[i];", "x[i] = o[i];"),
-    ("layerscale_dropped", "x[i] = x[i] + (real)W->ls1[i] * o[i];", "x[i] = x[i] + o[i];"),
+    ("layerscale_dropped", "x[i] = x[i] + (W->ls1 ? (real)W->ls1[i] * o[i] : o[i]);",
+     "x[i] = x[i] + o[i];"),
     ("swiglu_operands_swapped", "silu_r(g[i]) * u[i]", "silu_r(u[i]) * g[i]"),
     ("qnorm_uses_knorm", "rms_norm_r(q + hh * d, W->q_norm", "rms_norm_r(q + hh * d, W->k_norm"),
     ("final_norm_skipped", "rms_norm_r(x, m->final_norm, h, (real)c->norm_eps, y);",

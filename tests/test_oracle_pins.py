@@ -328,6 +328,21 @@ def test_ring_attention_empty_ring_first_step_returns_value():
     assert np.array_equal(out, vr[0].astype(np.float64))
 
 
+def test_unbounded_window_is_plain_causal_attention():
+    """window = ring >= every position (the FlowLM backbone): nothing is masked but the empty
+    slots, so ring attention equals plain attention over the filled history."""
+    r = _rng(13)
+    ring, H, d, L = 40, 4, 64, 29
+    pr = np.full(ring, oracle.INVALID_POS, np.uint32)
+    pr[:L] = np.arange(L)
+    q = r.standard_normal((H, d)).astype(np.float32)
+    kr = r.standard_normal((ring, H, d)).astype(np.float32)
+    vr = r.standard_normal((ring, H, d)).astype(np.float32)
+    got = oracle.ring_attention(q, kr, vr, pr, ring, L - 1, "f64")
+    want = oracle.gqa_attention(q, kr[:L], vr[:L], "f64")
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
 # ------------------------------------------------------------------------ the stack
 
 def _f32(a):
@@ -379,6 +394,38 @@ def test_prefill_is_causal_steps_of_pinned_primitives():
     assert m.length(0) == 36
     with pytest.raises(ValueError):  # 36 + 5 > max_pos
         m.prefill(0, np.zeros((5, w.hidden), np.float32))
+
+
+def test_flowlm_head_is_layer_norm_then_eos_of_pinned_primitives():
+    """The FlowLM backbone's head: the step output is out_norm(x) of the last layer's residual
+    stream (the last tap) and the EOS logit is eos_w . out plus its bias."""
+    w = W.SMALL_FLOWLM
+    syn = W.generate(w)
+    m = oracle.OracleModel(syn)
+    hd = syn.head
+    for t in range(3):
+        pos = [m.length(s) for s in range(w.streams)]
+        out, taps = m.step(syn.inputs[t], pos, taps=True)
+        for s in range(w.streams):
+            want = _f32(oracle.layer_norm(_f32(taps[-1][s]), hd["norm_w"], hd["norm_b"], w.norm_eps))
+            assert np.array_equal(out[s], want.astype(np.float64))
+            e = np.float32(0)
+            for i in range(w.hidden):  # ascending, in f32
+                e = np.float32(e + np.float32(hd["eos_w"][i]) * np.float32(want[i]))
+            assert m.eos(s) == float(e) + float(hd["eos_b"][0])
+
+
+def test_missing_layer_scale_is_a_scale_of_one():
+    """A codec layer without LayerScale (FlowLM) equals one with LayerScale vectors of ones."""
+    import dataclasses
+    syn = W.generate(W.SMALL_FLOWLM)
+    ones = dataclasses.replace(syn, layers=[dict(d, ls1=np.ones(W.SMALL_FLOWLM.hidden, np.float32),
+                                                 ls2=np.ones(W.SMALL_FLOWLM.hidden, np.float32))
+                                            for d in syn.layers])
+    a, b = oracle.OracleModel(syn), oracle.OracleModel(ones)
+    for t in range(3):
+        pos = [a.length(s) for s in range(W.SMALL_FLOWLM.streams)]
+        assert np.array_equal(a.step(syn.inputs[t], pos), b.step(syn.inputs[t], pos))
 
 
 def test_talker_step_is_the_page_order_of_pinned_primitives():

@@ -21,7 +21,7 @@ DEC_FLAG_TAPS, DEC_FLAG_NO_GRAPH, DEC_FLAG_PERSISTENT = 1, 2, 4
 
 # every symbol include/dec.h declares
 EXPORTS = ("dec_create", "dec_destroy", "dec_last_error", "dec_set_stream", "dec_prefill_kv",
-           "dec_prefill", "dec_prefill_block_rows", "dec_step", "dec_step_host", "dec_reset", "dec_sync", "dec_get_len", "dec_read_kv",
+           "dec_prefill", "dec_prefill_block_rows", "dec_read_eos", "dec_step", "dec_step_host", "dec_reset", "dec_sync", "dec_get_len", "dec_read_kv",
            "dec_read_tap", "dec_kernels_per_step", "dec_truncate", "dec_launch_stage",
            "dec_gemv", "dec_attention_workspace_bytes", "dec_attention",
            "dec_attention_noalloc")
@@ -46,7 +46,8 @@ class DecLayerWeights(C.Structure):
 
 
 class DecWeights(C.Structure):
-    _fields_ = [("layers", C.POINTER(DecLayerWeights)), ("final_norm", C.c_void_p)]
+    _fields_ = [("layers", C.POINTER(DecLayerWeights)), ("final_norm", C.c_void_p),
+                ("final_norm_b", C.c_void_p), ("eos_w", C.c_void_p), ("eos_b", C.c_float)]
 
 
 class DecError(RuntimeError):
@@ -80,6 +81,7 @@ def load() -> C.CDLL:
         L.dec_prefill_kv.argtypes = [vp, i32, vp, vp, i32]
         L.dec_prefill.argtypes = [vp, i32, i32, vp, vp]
         L.dec_prefill_block_rows.argtypes = [vp]
+        L.dec_read_eos.argtypes = [vp, i32, vp]
         L.dec_prefill_block_rows.restype = i32
         L.dec_step.argtypes = [vp, i32, vp, C.POINTER(C.c_int32), vp]
         L.dec_step_host.argtypes = [vp, i32, vp, C.POINTER(C.c_int32), vp]
@@ -99,7 +101,7 @@ def load() -> C.CDLL:
         for f in ("dec_set_stream", "dec_prefill_kv", "dec_step", "dec_step_host", "dec_reset",
                   "dec_sync", "dec_read_kv", "dec_read_tap", "dec_gemv", "dec_attention",
                   "dec_attention_noalloc",
-                  "dec_truncate", "dec_launch_stage"):
+                  "dec_truncate", "dec_launch_stage", "dec_prefill", "dec_read_eos"):
             getattr(L, f).restype = i32
         L.dec_get_len.restype = i32
         L.dec_kernels_per_step.restype = i32

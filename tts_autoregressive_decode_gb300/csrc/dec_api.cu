@@ -106,6 +106,10 @@ struct dec_ctx {
     char* arena = nullptr;  // weights
     std::vector<LayerW> L;
     const float* final_norm = nullptr;
+    const float* final_norm_b = nullptr;  // codec head: out_norm bias
+    const float* eos_w = nullptr;         // codec head: EOS row
+    float eos_b = 0.f;
+    float* eos = nullptr;                 // [S] the last step's EOS logits (no bias)
     char* state = nullptr;  // caches, tables, scratch
     float *kc = nullptr, *vc = nullptr;
     uint32_t* pr = nullptr;
@@ -348,7 +352,10 @@ FinalParams final_params(dec_ctx* ctx, int m, float* out) {
     f.m = m;
     f.h = c.hidden;
     f.x = ctx->xres;
-    f.w = c.kind == DEC_QWEN3_TALKER ? ctx->final_norm : nullptr;
+    f.w = ctx->final_norm;  // talker RMSNorm; codec: the head's LayerNorm, or NULL (copy)
+    f.b = ctx->final_norm_b;
+    f.eos_w = ctx->eos_w;
+    f.eos = ctx->eos;
     f.eps = c.norm_eps;
     f.out = out;
     f.len = ctx->len_dev;
@@ -606,7 +613,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
         const void* need_t[] = {lw.q, lw.k, lw.v, lw.o, lw.gate, lw.up, lw.down,
                                 lw.in_norm, lw.q_norm, lw.k_norm, lw.post_norm};
         const void* need_c[] = {lw.in_proj, lw.out_proj, lw.lin1, lw.lin2, lw.ln1_w,
-                                lw.ln1_b, lw.ln2_w, lw.ln2_b, lw.ls1, lw.ls2};
+                                lw.ln1_b, lw.ln2_w, lw.ln2_b};  // ls1 / ls2 optional
         if (talker) {
             for (const void* p : need_t)
                 if (!p) return fail(nullptr, DEC_E_ARG, "layer %d: a talker weight is NULL", l);
@@ -616,6 +623,8 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
         }
     }
     if (talker && !w->final_norm) return fail(nullptr, DEC_E_ARG, "final_norm is NULL");
+    if (!talker && w->final_norm && !w->final_norm_b)
+        return fail(nullptr, DEC_E_ARG, "codec final_norm (LayerNorm) needs final_norm_b");
 
     dec_ctx* ctx = new dec_ctx();
     ctx->cfg = c;
@@ -678,7 +687,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
             for (int j = 0; j < 6; ++j) o.f[j] = take(h * 4);
         }
     }
-    const size_t fn_off = take(h * 4);
+    const size_t fn_off = take(h * 4), fnb_off = take(h * 4), eos_off = take(h * 4);
     if ((e = cudaMalloc(&ctx->arena, tot)) != cudaSuccess) return bail(cuda_fail(ctx, e, "weight arena"));
     cudaStream_t s = ctx->stream;
     auto cp = [&](size_t off, const void* src, size_t bytes) {
@@ -723,21 +732,32 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
                 (e = cp(o.dd, lw.lin2, (size_t)h * I * es)) != cudaSuccess)
                 return bail(cuda_fail(ctx, e, "weight copy"));
             for (int j = 0; j < 6; ++j)
-                if ((e = cp(o.f[j], vecs[j], h * 4)) != cudaSuccess)
+                if (vecs[j] && (e = cp(o.f[j], vecs[j], h * 4)) != cudaSuccess)
                     return bail(cuda_fail(ctx, e, "weight copy"));
             L.in_proj = ctx->arena + o.a;
             L.out_proj = ctx->arena + o.b;
             L.lin1 = ctx->arena + o.cc;
             L.lin2 = ctx->arena + o.dd;
             const float** dst[6] = {&L.ln1_w, &L.ln1_b, &L.ln2_w, &L.ln2_b, &L.ls1, &L.ls2};
-            for (int j = 0; j < 6; ++j)
-                *dst[j] = reinterpret_cast<const float*>(ctx->arena + o.f[j]);
+            for (int j = 0; j < 6; ++j)  // a missing LayerScale stays NULL (a scale of one)
+                *dst[j] = vecs[j] ? reinterpret_cast<const float*>(ctx->arena + o.f[j]) : nullptr;
         }
     }
-    if (talker) {
+    if (w->final_norm) {  // talker: final RMSNorm; codec: the FlowLM head's out_norm
         if ((e = cp(fn_off, w->final_norm, h * 4)) != cudaSuccess)
             return bail(cuda_fail(ctx, e, "weight copy"));
         ctx->final_norm = reinterpret_cast<const float*>(ctx->arena + fn_off);
+    }
+    if (!talker && w->final_norm) {
+        if ((e = cp(fnb_off, w->final_norm_b, h * 4)) != cudaSuccess)
+            return bail(cuda_fail(ctx, e, "weight copy"));
+        ctx->final_norm_b = reinterpret_cast<const float*>(ctx->arena + fnb_off);
+    }
+    if (!talker && w->eos_w) {
+        if ((e = cp(eos_off, w->eos_w, h * 4)) != cudaSuccess)
+            return bail(cuda_fail(ctx, e, "weight copy"));
+        ctx->eos_w = reinterpret_cast<const float*>(ctx->arena + eos_off);
+        ctx->eos_b = w->eos_b;
     }
 
     // ---- state: caches, stamps, tables, scratch -------------------------------------------------
@@ -760,6 +780,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     const size_t o_part = take(attention_part_bytes(R, H, ctx->max_chunks, d));
     const size_t o_ml = take(attention_ml_bytes(R, H, ctx->max_chunks));
     const size_t o_len = take((size_t)S * 4), o_st = take(4), o_gbar = take(sizeof(GridBarrier));
+    const size_t o_eos = take((size_t)S * 4);
     const size_t o_taps = (c.flags & DEC_FLAG_TAPS) ? take((size_t)c.layers * S * h * 4) : 0;
     const size_t o_in = take((size_t)S * h * 4), o_out = take((size_t)S * h * 4);
     if ((e = cudaMalloc(&ctx->state, tot)) != cudaSuccess) return bail(cuda_fail(ctx, e, "state"));
@@ -778,6 +799,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->len_dev = reinterpret_cast<int32_t*>(b + o_len);
     ctx->status = reinterpret_cast<unsigned*>(b + o_st);
     ctx->gbar = reinterpret_cast<GridBarrier*>(b + o_gbar);
+    ctx->eos = reinterpret_cast<float*>(b + o_eos);
     ctx->taps = (c.flags & DEC_FLAG_TAPS) ? reinterpret_cast<float*>(b + o_taps) : nullptr;
     ctx->io_in = reinterpret_cast<float*>(b + o_in);
     ctx->io_out = reinterpret_cast<float*>(b + o_out);
@@ -888,6 +910,16 @@ dec_status dec_prefill(dec_ctx* ctx, int stream, int n, const float* x, float* o
 }
 
 int dec_prefill_block_rows(const dec_ctx* ctx) { return ctx ? ctx->prefill_rows : 0; }
+
+dec_status dec_read_eos(dec_ctx* ctx, int m, float* dst_host) {
+    if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");
+    if (!ctx->eos_w) return fail(ctx, DEC_E_UNSUPPORTED, "the context has no EOS row");
+    if (m < 1 || m > ctx->S || !dst_host) return fail(ctx, DEC_E_ARG, "bad m or NULL dst");
+    CUDA_TRY(ctx, cudaStreamSynchronize(ctx->stream), "stream sync");
+    CUDA_TRY(ctx, cudaMemcpy(dst_host, ctx->eos, (size_t)m * 4, cudaMemcpyDeviceToHost), "eos read");
+    for (int i = 0; i < m; ++i) dst_host[i] += ctx->eos_b;
+    return DEC_OK;
+}
 
 dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, float* hidden_out) {
     if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");

@@ -118,7 +118,10 @@ size_t attention_ml_bytes(int m, int H, int max_chunks);
 struct FinalParams {
     int m, h;
     const float* x;        // residual stream [m][h]
-    const float* w;        // talker final norm [h]; null = copy (codec)
+    const float* w;        // final norm weight [h]: RMSNorm, or LayerNorm with b; null = copy
+    const float* b;        // LayerNorm bias [h] (codec head), or null
+    const float* eos_w;    // EOS row [h] (codec head), or null
+    float* eos;            // [m] eos_w . out, when eos_w
     float eps;
     float* out;            // [m][h]
     int32_t* len;          // [m]: incremented (row r advances stream r) ...

@@ -57,7 +57,8 @@ class Decoder:
 
     def __init__(self, cfg: L.DecConfig, layers: List[Dict[str, torch.Tensor]],
                  final_norm: Optional[torch.Tensor] = None,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None,
+                 head: Optional[Dict[str, torch.Tensor]] = None, eos_b: float = 0.0):
         self.lib = L.load()
         self.cfg = cfg
         arr = (L.DecLayerWeights * cfg.layers)()
@@ -65,6 +66,11 @@ class Decoder:
             for name, t in d.items():
                 setattr(arr[i], name, _ptr(t))
         w = L.DecWeights(layers=arr, final_norm=_ptr(final_norm) if final_norm is not None else None)
+        if head is not None:  # codec: the FlowLM backbone's out_norm and EOS row
+            w.final_norm = _ptr(head["norm_w"])
+            w.final_norm_b = _ptr(head["norm_b"])
+            w.eos_w = _ptr(head["eos_w"])
+            w.eos_b = float(eos_b)
         h = C.c_void_p()
         st = self.lib.dec_create(C.byref(cfg), C.byref(w), _stream_handle(stream), C.byref(h))
         L.check(st, None)
@@ -81,8 +87,12 @@ class Decoder:
         names = _TALKER_MAP if w.kind == "talker" else _CODEC_MAP
         layers = [{names[k]: to_device(v, device) for k, v in d.items()} for d in syn.layers]
         fn = to_device(syn.final_norm, device) if syn.final_norm is not None else None
-        dec = cls(cfg, layers, fn, stream)
-        del layers, fn   # the context holds its own copy of the weights
+        head = None
+        if getattr(syn, "head", None) is not None:
+            head = {k: to_device(syn.head[k], device) for k in ("norm_w", "norm_b", "eos_w")}
+        eos_b = float(syn.head["eos_b"][0]) if head is not None else 0.0
+        dec = cls(cfg, layers, fn, stream, head, eos_b)
+        del layers, fn, head   # the context holds its own copy of the weights
         if prefill:
             for s, n in enumerate(syn.lengths):
                 if n > 0:
@@ -107,6 +117,12 @@ class Decoder:
         if out is None:
             out = torch.empty_like(x)
         L.check(self.lib.dec_prefill(self.h, stream, n, _ptr(x), _ptr(out)), self.h)
+        return out
+
+    def read_eos(self, m: int) -> np.ndarray:
+        """The EOS logits of the last step of streams 0..m-1 (bias included); blocking."""
+        out = np.empty(m, np.float32)
+        L.check(self.lib.dec_read_eos(self.h, m, out.ctypes.data), self.h)
         return out
 
     def prefill_rows(self) -> int:

@@ -1,15 +1,18 @@
 """Synthetic, seeded decode workloads: shapes, value distributions and draw order.
 
-This module holds no arithmetic of the decode step.  It only states the five workload
-shapes and draws their inputs, so that the CUDA library and the CPU oracle consume the
-very same bytes.
+This module holds no arithmetic of the decode step.  It only states the workload shapes and
+draws their inputs, so that the CUDA library and the CPU oracle consume the very same bytes.
 
 Draw recipe (numpy PCG64; one child stream per category, spawned from the seed with
 ``np.random.SeedSequence(seed).spawn(4)`` so that one category never shifts another):
 
   child 0  stream lengths   -- only where lengths are random: integers in [lo, hi], inclusive
   child 1  weights          -- layer by layer, tensor by tensor in the order of
-                               ``TALKER_TENSORS`` / ``CODEC_TENSORS``, then the final norm
+                               ``TALKER_TENSORS`` / ``CODEC_TENSORS`` (the codec's LayerScale
+                               only where the workload has it), then the talker's final norm,
+                               or the codec head where the workload has one: out_norm weight,
+                               out_norm bias, EOS weights [hidden] (linear), EOS bias (scalar,
+                               0.01 N(0, 1))
            linear weights   N(0, 1) float32 draws times 0.02 (in float32)
            norm weights     1 + 0.01 N(0, 1)
            LayerNorm biases 0.01 N(0, 1)
@@ -57,6 +60,8 @@ class Workload:
     ring: int = 0             # codec ring slots
     window: int = 0           # codec attention window
     max_pos: int = 0          # 0: derived (longest prefill + steps)
+    layer_scale: bool = True  # codec: LayerScale on both residual branches
+    head: bool = False        # codec: final LayerNorm and an EOS logit (the FlowLM backbone)
     description: str = ""
 
     @property
@@ -74,9 +79,11 @@ class Workload:
                     "wo": (h, self.qw), "wgate": (I, h), "wup": (I, h), "wdown": (h, I),
                     "in_norm": (h,), "q_norm": (self.head_dim,), "k_norm": (self.head_dim,),
                     "post_norm": (h,)}
-        return {"in_proj": (3 * h, h), "out_proj": (h, h), "lin1": (I, h), "lin2": (h, I),
-                "ln1_w": (h,), "ln1_b": (h,), "ln2_w": (h,), "ln2_b": (h,),
-                "ls1": (h,), "ls2": (h,)}
+        shapes = {"in_proj": (3 * h, h), "out_proj": (h, h), "lin1": (I, h), "lin2": (h, I),
+                  "ln1_w": (h,), "ln1_b": (h,), "ln2_w": (h,), "ln2_b": (h,)}
+        if self.layer_scale:
+            shapes.update({"ls1": (h,), "ls2": (h,)})
+        return shapes
 
     def matrix_bytes(self) -> int:
         es = 2 if self.weight_dtype == "bf16" else 4
@@ -123,6 +130,7 @@ class Synthetic:
     x0: Optional[np.ndarray] = None           # feedback: [streams][hidden]
     e: Optional[np.ndarray] = None            # feedback: [hidden]
     max_pos: int = 0
+    head: Optional[Dict[str, np.ndarray]] = None  # codec head: norm_w, norm_b, eos_w, eos_b
 
 
 def _normal(rng, shape) -> np.ndarray:
@@ -140,6 +148,8 @@ def generate(w: Workload, steps: Optional[int] = None, with_inputs: bool = True)
     for _ in range(w.layers):
         d = {}
         for name in order:
+            if name not in shapes:
+                continue
             s = shapes[name]
             if len(s) == 2:
                 a = _normal(rw, s) * np.float32(0.02)
@@ -151,9 +161,14 @@ def generate(w: Workload, steps: Optional[int] = None, with_inputs: bool = True)
             else:
                 d[name] = np.float32(1.0) + _normal(rw, s) * np.float32(0.01)
         layers.append(d)
-    final_norm = None
+    final_norm = head = None
     if w.kind == "talker":
         final_norm = np.float32(1.0) + _normal(rw, (w.hidden,)) * np.float32(0.01)
+    elif w.head:
+        head = {"norm_w": np.float32(1.0) + _normal(rw, (w.hidden,)) * np.float32(0.01),
+                "norm_b": _normal(rw, (w.hidden,)) * np.float32(0.01),
+                "eos_w": _normal(rw, (w.hidden,)) * np.float32(0.02),
+                "eos_b": _normal(rw, (1,)) * np.float32(0.01)}
 
     rk = np.random.Generator(np.random.PCG64(c[2]))
     pk, pv = [], []
@@ -174,11 +189,11 @@ def generate(w: Workload, steps: Optional[int] = None, with_inputs: bool = True)
             e = _normal(ri, (w.hidden,))
         else:
             inputs = _normal(ri, (nsteps, w.streams, w.hidden))
-    return Synthetic(w, layers, final_norm, lengths, pk, pv, inputs, x0, e, max_pos(w))
+    return Synthetic(w, layers, final_norm, lengths, pk, pv, inputs, x0, e, max_pos(w), head)
 
 
 # ----------------------------------------------------------------------------------------
-# the five workloads
+# the workloads
 # ----------------------------------------------------------------------------------------
 
 TALKER_H256_L1 = Workload(
@@ -217,8 +232,21 @@ TALKER_H2048_L28_M8 = Workload(
     description="batched decode of 8 streams sharing one read of each weight; 28-layer "
                 "bf16 talker; per-stream f32 KV prefilled to lengths U[512, 4096]; 64 steps")
 
+# The FlowLM backbone shape (Pocket TTS on wgpu, PocketBackboneGpu): the codec-style stack
+# without LayerScale and with an unbounded window (window = ring = the utterance's positions),
+# then the final LayerNorm and the EOS logit.  The FFN width is not on the pages: 4 x d_model.
+FLOWLM_D1024_L6 = Workload(
+    name="flowlm_d1024_l6", kind="codec", layers=6, hidden=1024, q_heads=16, kv_heads=16,
+    head_dim=64, inter=4096, norm_eps=1e-5, rope_theta=1e4, weight_dtype="f32", streams=1,
+    steps=64, seed=5, prefill=(256,), ring=320, window=320, max_pos=320, layer_scale=False,
+    head=True,
+    description="FlowLM backbone: 6 layers f32, d1024, 16 heads MHA d64, LayerNorm, GELU(erf) "
+                "MLP 4096, no LayerScale, unbounded window (ring = window = 320 positions), "
+                "final LayerNorm + EOS logit; 256 prefilled positions (a voice), 64 steps")
+
 WORKLOADS: Dict[str, Workload] = {w.name: w for w in (
-    TALKER_H256_L1, TALKER_H1024_L4, TALKER_H2048_L28, CODEC_D512_L8, TALKER_H2048_L28_M8)}
+    TALKER_H256_L1, TALKER_H1024_L4, TALKER_H2048_L28, CODEC_D512_L8, TALKER_H2048_L28_M8,
+    FLOWLM_D1024_L6)}
 
 # Small shapes for element-by-element parity: several tiles and a ragged tail everywhere
 # (hidden and inter not multiples of the 256-element warp step, prefills not multiples of
@@ -235,5 +263,9 @@ SMALL_CODEC = Workload(
     head_dim=64, inter=520, norm_eps=1e-5, rope_theta=1e4, weight_dtype="f32", streams=2,
     steps=45, seed=13, ring=20, window=17, prefill=(0, 9), max_pos=64)
 
+SMALL_FLOWLM = dataclasses.replace(
+    SMALL_CODEC, name="small_flowlm", seed=14, ring=40, window=40, max_pos=40, prefill=(7, 0),
+    steps=30, layer_scale=False, head=True)
+
 SMALL: Dict[str, Workload] = {w.name: w for w in (SMALL_TALKER_F32, SMALL_TALKER_BF16,
-                                                  SMALL_CODEC)}
+                                                  SMALL_CODEC, SMALL_FLOWLM)}
