@@ -410,6 +410,33 @@ def run_ours(args):
                    "bytes": pbytes, "position": base[0],
                    "note": "weights read once per block of block_rows rows"}
 
+    # ---- the flow head on the backbone's hidden state (FlowLM-shaped workloads) ------------------
+    flow = None
+    if w.head and W.FLOW_D512.cond == w.hidden:
+        from tts_autoregressive_decode_gb300.decoder import FlowHead
+        fs = W.FLOW_D512
+        fw = W.generate_flow(fs, calls=1)
+        head = FlowHead(fs, fw)
+        noise = torch.from_numpy(fw["noise"][0]).cuda()
+        lat = torch.empty_like(noise)
+        for _ in range(10):
+            head.step(out[0], noise, lat)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(200):
+            head.step(out[0], noise, lat)
+        b.record(stream)
+        torch.cuda.synchronize()
+        fus = a.elapsed_time(b) / 200 * 1e3
+        D_, L_, C_, B_ = fs.dim, fs.latent, fs.cond, fs.blocks
+        fbytes = 4 * (D_ * L_ + D_ * C_ + (3 * B_ + 2) * D_ * D_ + 2 * B_ * D_ * D_ + L_ * D_)
+        flow = {"shape": fs.name, "us_per_call": fus, "kernels": head.kernels_per_step(),
+                "weight_bytes": fbytes, "achieved_hbm_gbs": fbytes / (fus * 1e-6) / 1e9,
+                "note": "one LSD step conditioned in place on the step's output row"}
+        head.close()
+
     # ---- end to end through the C ABI with host buffers ----------------------------------------
     e2e = None
     if not args.no_e2e:
@@ -473,7 +500,7 @@ def run_ours(args):
         "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                           "frac": step_gbs / peak, "bytes_per_step": nb},
         "gpu_launches": launches,
-        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "prefill": prefill,
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "prefill": prefill, "flow_head": flow,
     }
     print(json.dumps(line))
     if pg:

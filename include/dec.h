@@ -240,6 +240,56 @@ dec_status dec_truncate(dec_ctx* ctx, int stream, int new_len);
 dec_status dec_launch_stage(dec_ctx* ctx, int layer, int stage, int m);
 
 /* ---------------------------------------------------------------------------------------
+ * The flow head (Pocket TTS on wgpu, PocketFlowGpu: SimpleMLPAdaLN, one LSD step), reading
+ * the backbone's hidden state in place on the device.  One call:
+ *   x = W_ip noise + b_ip;  y = silu(t_const + W_c cond + b_c)
+ *   per block: (shift, scale, gate) = W_ada y + b_ada;
+ *              x += gate * (W_2 silu(W_0 (LN(x; ln_w, ln_b) (1 + scale) + shift) + b_0) + b_2)
+ *   final:     (shift, scale) = W_fada y + b_fada;
+ *              latent = noise + W_f (LN(x; 1, 0) (1 + scale) + shift) + b_f
+ * All weights f32, row-major [out][in], 16-byte aligned DEVICE pointers; the per-block fields
+ * are HOST arrays of `blocks` DEVICE pointers.  dec_flow_create copies them.
+ * ------------------------------------------------------------------------------------- */
+typedef struct {
+    int dim;        /* the head's width (multiple of 8) */
+    int latent;     /* latent / noise width (multiple of 8) */
+    int cond;       /* conditioning width: the backbone's hidden (multiple of 8) */
+    int blocks;     /* residual blocks (>= 0) */
+    float ln_eps;   /* LayerNorm eps (1e-6 on the page) */
+    int lsd_steps;  /* must be 1: the page plans one LSD step */
+} dec_flow_config;
+
+typedef struct {
+    const float *ip_w, *ip_b;        /* input_proj [dim][latent], [dim] */
+    const float *cond_w, *cond_b;    /* cond embedding [dim][cond], [dim] */
+    const float* t_const;            /* constant timestep embedding [dim] */
+    const float* const* ada_w;       /* [blocks] of [3 dim][dim]: shift | scale | gate rows */
+    const float* const* ada_b;       /* [blocks] of [3 dim] */
+    const float* const* ln_w;        /* [blocks] of [dim] */
+    const float* const* ln_b;
+    const float* const* m0_w;        /* [blocks] of [dim][dim] (SiLU after) */
+    const float* const* m0_b;
+    const float* const* m2_w;        /* [blocks] of [dim][dim] */
+    const float* const* m2_b;
+    const float *fada_w, *fada_b;    /* final adaLN [2 dim][dim] (shift | scale), [2 dim] */
+    const float *f_w, *f_b;          /* final linear [latent][dim], [latent] */
+} dec_flow_weights;
+
+typedef struct dec_flow dec_flow;
+
+/* Errors: DEC_E_ARG (NULL, bad sizes), DEC_E_UNSUPPORTED (lsd_steps != 1, widths not multiples
+ * of 8), DEC_E_CUDA.  On failure *out is NULL and dec_flow_last_error(NULL) tells why. */
+dec_status dec_flow_create(const dec_flow_config* cfg, const dec_flow_weights* w, void* stream,
+                           dec_flow** out);
+/* One LSD step on the head's stream: cond DEVICE [cond] (e.g. a dec_step hidden_out row, read
+ * in place), noise DEVICE [latent], latent_out DEVICE [latent] (may not overlap noise).
+ * Asynchronous; captured as a CUDA graph per (cond, noise, latent_out) and replayed. */
+dec_status dec_flow_step(dec_flow* f, const float* cond, const float* noise, float* latent_out);
+void dec_flow_destroy(dec_flow* f);
+const char* dec_flow_last_error(const dec_flow* f);
+int dec_flow_kernels_per_step(const dec_flow* f);
+
+/* ---------------------------------------------------------------------------------------
  * Stateless kernel entry points (the same kernels the step uses, on caller buffers).
  * ------------------------------------------------------------------------------------- */
 

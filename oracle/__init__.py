@@ -70,6 +70,7 @@ def lib(precision: str = "f32") -> C.CDLL:
         L.orc_prefill_kv.argtypes = [C.c_void_p, C.c_int, _fp, _fp, C.c_int]
         L.orc_step.argtypes = [C.c_void_p, C.c_int, _fp, C.POINTER(C.c_int), _dp, _dp]
         L.orc_prefill.argtypes = [C.c_void_p, C.c_int, C.c_int, _fp, _dp]
+        L.orc_flow_step.argtypes = [C.c_void_p, _fp, _fp, _dp]
         L.orc_set_head.argtypes = [C.c_void_p, _fp, _fp, _fp]
         L.orc_eos.argtypes = [C.c_void_p, C.c_int]
         L.orc_eos.restype = C.c_double
@@ -184,6 +185,54 @@ def gqa_attention(q, kc, vc, precision: str = "f32") -> np.ndarray:
     out = np.empty((H, d), np.float64)
     lib(precision).orc_gqa_attention(_ptr(q, C.c_double), _ptr(kc, C.c_double),
                                      _ptr(vc, C.c_double), L, H, G, d, _ptr(out, C.c_double))
+    return out
+
+
+class OrcFlow(C.Structure):
+    _fields_ = [("dim", C.c_int), ("latent", C.c_int), ("cond", C.c_int), ("blocks", C.c_int),
+                ("ln_eps", C.c_double),
+                ("ip_w", C.c_void_p), ("ip_b", C.c_void_p), ("cond_w", C.c_void_p),
+                ("cond_b", C.c_void_p), ("t_const", C.c_void_p),
+                ("ada_w", C.c_void_p), ("ada_b", C.c_void_p), ("ln_w", C.c_void_p),
+                ("ln_b", C.c_void_p), ("m0_w", C.c_void_p), ("m0_b", C.c_void_p),
+                ("m2_w", C.c_void_p), ("m2_b", C.c_void_p),
+                ("fada_w", C.c_void_p), ("fada_b", C.c_void_p), ("f_w", C.c_void_p),
+                ("f_b", C.c_void_p)]
+
+
+def flow_step(shape, weights: Dict[str, np.ndarray], cond, noise,
+              precision: str = "f32") -> np.ndarray:
+    """One LSD step of the flow head (`shape`: dim, latent, cond, blocks, ln_eps; `weights` as
+    workloads.generate_flow draws them) for one conditioning row and one noise row."""
+    keep = []
+
+    def arr(a):
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        keep.append(a)
+        return a.ctypes.data
+
+    def per_block(name):
+        ptrs = (C.c_void_p * max(1, shape.blocks))(*[arr(weights[f"{name}{i}"])
+                                                     for i in range(shape.blocks)])
+        keep.append(ptrs)
+        return C.cast(ptrs, C.c_void_p).value
+
+    f = OrcFlow(dim=shape.dim, latent=shape.latent, cond=shape.cond, blocks=shape.blocks,
+                ln_eps=shape.ln_eps,
+                ip_w=arr(weights["ip_w"]), ip_b=arr(weights["ip_b"]),
+                cond_w=arr(weights["cond_w"]), cond_b=arr(weights["cond_b"]),
+                t_const=arr(weights["t_const"]),
+                ada_w=per_block("ada_w"), ada_b=per_block("ada_b"), ln_w=per_block("ln_w"),
+                ln_b=per_block("ln_b"), m0_w=per_block("m0_w"), m0_b=per_block("m0_b"),
+                m2_w=per_block("m2_w"), m2_b=per_block("m2_b"),
+                fada_w=arr(weights["fada_w"]), fada_b=arr(weights["fada_b"]),
+                f_w=arr(weights["f_w"]), f_b=arr(weights["f_b"]))
+    c = np.ascontiguousarray(cond, dtype=np.float32)
+    n = np.ascontiguousarray(noise, dtype=np.float32)
+    out = np.empty(shape.latent, np.float64)
+    if lib(precision).orc_flow_step(C.byref(f), _ptr(c, C.c_float), _ptr(n, C.c_float),
+                                    _ptr(out, C.c_double)):
+        raise ValueError("orc_flow_step rejected its arguments")
     return out
 
 

@@ -626,6 +626,54 @@ int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* 
     return 0;
 }
 
+int orc_flow_step(const orc_flow* f, const float* cond, const float* noise, double* out) {
+    if (!f || !cond || !noise || !out || f->dim < 1 || f->latent < 1 || f->cond < 1 ||
+        f->blocks < 0)
+        return -1;
+    const int D = f->dim, Lt = f->latent, C = f->cond;
+    const real eps = (real)f->ln_eps;
+    real* x = (real*)malloc(sizeof(real) * (size_t)D);
+    real* y = (real*)malloc(sizeof(real) * (size_t)D);
+    real* m = (real*)malloc(sizeof(real) * 3 * (size_t)D);
+    real* u = (real*)malloc(sizeof(real) * (size_t)D);
+    real* t = (real*)malloc(sizeof(real) * (size_t)(D > C ? D : C));
+    real* h = (real*)malloc(sizeof(real) * (size_t)D);
+    float* one = (float*)malloc(sizeof(float) * (size_t)D);
+    float* zero = (float*)malloc(sizeof(float) * (size_t)D);
+    real* dir = (real*)malloc(sizeof(real) * (size_t)Lt);
+    for (int i = 0; i < D; ++i) {
+        one[i] = 1.0f;
+        zero[i] = 0.0f;
+    }
+    /* x = input_proj(noise) */
+    for (int i = 0; i < Lt; ++i) t[i] = (real)noise[i];
+    matvec_r(f->ip_w, 0, D, Lt, t, x);
+    for (int i = 0; i < D; ++i) x[i] += (real)f->ip_b[i];
+    /* y = silu(t_const + cond_embed(cond)) */
+    for (int i = 0; i < C; ++i) t[i] = (real)cond[i];
+    matvec_r(f->cond_w, 0, D, C, t, y);
+    for (int i = 0; i < D; ++i) y[i] = silu_r((real)f->t_const[i] + (y[i] + (real)f->cond_b[i]));
+    for (int bl = 0; bl < f->blocks; ++bl) {
+        matvec_r(f->ada_w[bl], 0, 3 * D, D, y, m);
+        for (int i = 0; i < 3 * D; ++i) m[i] += (real)f->ada_b[bl][i];
+        layer_norm_r(x, f->ln_w[bl], f->ln_b[bl], D, eps, u);
+        for (int i = 0; i < D; ++i) u[i] = u[i] * ((real)1 + m[D + i]) + m[i];  /* modulate */
+        matvec_r(f->m0_w[bl], 0, D, D, u, h);
+        for (int i = 0; i < D; ++i) h[i] = silu_r(h[i] + (real)f->m0_b[bl][i]);
+        matvec_r(f->m2_w[bl], 0, D, D, h, u);
+        for (int i = 0; i < D; ++i) x[i] += m[2 * D + i] * (u[i] + (real)f->m2_b[bl][i]);  /* gate */
+    }
+    matvec_r(f->fada_w, 0, 2 * D, D, y, m);
+    for (int i = 0; i < 2 * D; ++i) m[i] += (real)f->fada_b[i];
+    layer_norm_r(x, one, zero, D, eps, u);
+    for (int i = 0; i < D; ++i) u[i] = u[i] * ((real)1 + m[D + i]) + m[i];
+    matvec_r(f->f_w, 0, Lt, D, u, dir);
+    for (int i = 0; i < Lt; ++i)  /* the LSD update with one step: x1 = x0 + dir / 1 */
+        out[i] = (double)((real)noise[i] + (dir[i] + (real)f->f_b[i]) / (real)1);
+    free(x); free(y); free(m); free(u); free(t); free(h); free(one); free(zero); free(dir);
+    return 0;
+}
+
 int orc_prefill(orc_model* m, int stream, int n, const float* x_in, double* out) {
     if (!m || stream < 0 || stream >= m->c.streams || n < 1 || !x_in || !out) return -1;
     const orc_config* c = &m->c;

@@ -127,6 +127,33 @@ double orc_eos(const orc_model* m, int stream);
  * Returns 0, or < 0 on a bad argument or capacity. */
 int orc_prefill(orc_model* m, int stream, int n, const float* x_in, double* out);
 void orc_reset(orc_model* m, int stream);
+
+/* ---- the flow head (Pocket TTS on wgpu, PocketFlowGpu: SimpleMLPAdaLN, one LSD step) ---- */
+typedef struct {
+    int dim, latent, cond, blocks;
+    double ln_eps;
+    const float *ip_w, *ip_b;       /* input_proj [dim][latent], [dim] */
+    const float *cond_w, *cond_b;   /* cond embedding [dim][cond], [dim] */
+    const float* t_const;           /* the constant timestep embedding [dim] */
+    const float* const* ada_w;      /* per block: adaLN projection [3 dim][dim] = shift|scale|gate */
+    const float* const* ada_b;      /* [3 dim] */
+    const float* const* ln_w;       /* per block in_ln [dim] */
+    const float* const* ln_b;
+    const float* const* m0_w;       /* per block [dim][dim], [dim] (through SiLU) */
+    const float* const* m0_b;
+    const float* const* m2_w;
+    const float* const* m2_b;
+    const float *fada_w, *fada_b;   /* final adaLN [2 dim][dim] = shift|scale, [2 dim] */
+    const float *f_w, *f_b;         /* final linear [latent][dim], [latent] */
+} orc_flow;
+/* One LSD step (steps = 1) from `noise` [latent], conditioned on `cond` [cond]:
+ *   x = W_ip noise + b_ip;  y = silu(t_const + W_c cond + b_c)
+ *   per block: (shift, scale, gate) = W_ada y + b_ada; u = LN(x; w, b) (1 + scale) + shift;
+ *              x += gate * (W_2 silu(W_0 u + b_0) + b_2)
+ *   final: (shift, scale) = W_fada y + b_fada; u = LN(x; 1, 0) (1 + scale) + shift;
+ *   out = noise + (W_f u + b_f) / 1.
+ * Returns 0, or -1 on a bad argument. */
+int orc_flow_step(const orc_flow* f, const float* cond, const float* noise, double* out);
 int orc_len(const orc_model* m, int stream);
 /* read the stored key/value of (layer, stream, position) as [kv_heads][head_dim] */
 int orc_read_kv(const orc_model* m, int layer, int stream, int pos, double* k, double* v);

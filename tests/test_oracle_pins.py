@@ -428,6 +428,54 @@ def test_missing_layer_scale_is_a_scale_of_one():
         assert np.array_equal(a.step(syn.inputs[t], pos), b.step(syn.inputs[t], pos))
 
 
+def _flow_by_primitives(f, d, cond, noise):
+    """The flow head's LSD step composed from individually pinned oracle primitives, one
+    float32 rounding per operation, in the order of the page's dispatch plan."""
+    f32 = np.float32
+    sil = lambda v: _f32([oracle.silu(float(t)) for t in v])
+    x = _f32(oracle.matvec(d["ip_w"], noise)) + d["ip_b"]
+    y = sil(d["t_const"] + (_f32(oracle.matvec(d["cond_w"], cond)) + d["cond_b"]))
+    D = f.dim
+    for i in range(f.blocks):
+        m = _f32(oracle.matvec(d[f"ada_w{i}"], y)) + d[f"ada_b{i}"]
+        u = _f32(oracle.layer_norm(x, d[f"ln_w{i}"], d[f"ln_b{i}"], f.ln_eps))
+        u = u * (f32(1) + m[D:2 * D]) + m[:D]
+        h = sil(_f32(oracle.matvec(d[f"m0_w{i}"], u)) + d[f"m0_b{i}"])
+        x = x + m[2 * D:] * (_f32(oracle.matvec(d[f"m2_w{i}"], h)) + d[f"m2_b{i}"])
+    m = _f32(oracle.matvec(d["fada_w"], y)) + d["fada_b"]
+    u = _f32(oracle.layer_norm(x, np.ones(D, np.float32), np.zeros(D, np.float32), f.ln_eps))
+    u = u * (f32(1) + m[D:]) + m[:D]
+    return noise + (_f32(oracle.matvec(d["f_w"], u)) + d["f_b"]) / f32(1)
+
+
+def test_flow_head_is_the_page_order_of_pinned_primitives():
+    f = W.SMALL_FLOW
+    d = W.generate_flow(f)
+    for c in range(2):
+        got = oracle.flow_step(f, d, d["cond"][c], d["noise"][c])
+        want = _flow_by_primitives(f, d, d["cond"][c], d["noise"][c])
+        assert np.array_equal(got, want.astype(np.float64)), c
+
+
+def test_flow_head_with_zero_gates_skips_its_blocks():
+    """adaLN-Zero: with every gate zero the blocks leave x as input_proj made it, so the step
+    equals the head with no blocks."""
+    import dataclasses
+    f = W.SMALL_FLOW
+    d = W.generate_flow(f)
+    for i in range(f.blocks):
+        d[f"ada_w{i}"][2 * f.dim:] = 0
+        d[f"ada_b{i}"][2 * f.dim:] = 0
+    none = dataclasses.replace(f, blocks=0)
+    a = oracle.flow_step(f, d, d["cond"][0], d["noise"][0])
+    b = oracle.flow_step(none, d, d["cond"][0], d["noise"][0])
+    assert np.array_equal(a, b)
+    # and with a zero final linear the step returns the noise plus the final bias
+    d["f_w"][:] = 0
+    out = oracle.flow_step(f, d, d["cond"][0], d["noise"][0])
+    assert np.array_equal(out, (d["noise"][0] + d["f_b"]).astype(np.float64))
+
+
 def test_talker_step_is_the_page_order_of_pinned_primitives():
     w = W.TALKER_H256_L1
     syn = W.generate(w)

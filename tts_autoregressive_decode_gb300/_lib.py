@@ -24,7 +24,22 @@ EXPORTS = ("dec_create", "dec_destroy", "dec_last_error", "dec_set_stream", "dec
            "dec_prefill", "dec_prefill_block_rows", "dec_read_eos", "dec_step", "dec_step_host", "dec_reset", "dec_sync", "dec_get_len", "dec_read_kv",
            "dec_read_tap", "dec_kernels_per_step", "dec_truncate", "dec_launch_stage",
            "dec_gemv", "dec_attention_workspace_bytes", "dec_attention",
-           "dec_attention_noalloc")
+           "dec_attention_noalloc", "dec_flow_create", "dec_flow_step", "dec_flow_destroy",
+           "dec_flow_last_error", "dec_flow_kernels_per_step")
+
+
+class DecFlowConfig(C.Structure):
+    _fields_ = [("dim", C.c_int32), ("latent", C.c_int32), ("cond", C.c_int32),
+                ("blocks", C.c_int32), ("ln_eps", C.c_float), ("lsd_steps", C.c_int32)]
+
+
+FLOW_BLOCK_FIELDS = ("ada_w", "ada_b", "ln_w", "ln_b", "m0_w", "m0_b", "m2_w", "m2_b")
+
+
+class DecFlowWeights(C.Structure):
+    _fields_ = ([(n, C.c_void_p) for n in ("ip_w", "ip_b", "cond_w", "cond_b", "t_const")] +
+                [(n, C.POINTER(C.c_void_p)) for n in FLOW_BLOCK_FIELDS] +
+                [(n, C.c_void_p) for n in ("fada_w", "fada_b", "f_w", "f_b")])
 
 
 class DecConfig(C.Structure):
@@ -82,6 +97,17 @@ def load() -> C.CDLL:
         L.dec_prefill.argtypes = [vp, i32, i32, vp, vp]
         L.dec_prefill_block_rows.argtypes = [vp]
         L.dec_read_eos.argtypes = [vp, i32, vp]
+        L.dec_flow_create.argtypes = [C.POINTER(DecFlowConfig), C.POINTER(DecFlowWeights), vp,
+                                      C.POINTER(vp)]
+        L.dec_flow_create.restype = i32
+        L.dec_flow_step.argtypes = [vp, vp, vp, vp]
+        L.dec_flow_step.restype = i32
+        L.dec_flow_destroy.argtypes = [vp]
+        L.dec_flow_destroy.restype = None
+        L.dec_flow_last_error.argtypes = [vp]
+        L.dec_flow_last_error.restype = C.c_char_p
+        L.dec_flow_kernels_per_step.argtypes = [vp]
+        L.dec_flow_kernels_per_step.restype = i32
         L.dec_prefill_block_rows.restype = i32
         L.dec_step.argtypes = [vp, i32, vp, C.POINTER(C.c_int32), vp]
         L.dec_step_host.argtypes = [vp, i32, vp, C.POINTER(C.c_int32), vp]
@@ -112,4 +138,10 @@ def load() -> C.CDLL:
 def check(status: int, ctx=None) -> None:
     if status != DEC_OK:
         msg = load().dec_last_error(ctx).decode(errors="replace")
+        raise DecError(status, msg)
+
+
+def check_flow(status: int, head=None) -> None:
+    if status != DEC_OK:
+        msg = load().dec_flow_last_error(head).decode(errors="replace")
         raise DecError(status, msg)

@@ -335,6 +335,8 @@ static cudaError_t launch_rows_nj(const GemvParams& p, int nj, int num_sms, cuda
 
 cudaError_t launch_gemv(const GemvParams& p, int dtype, int num_sms, cudaStream_t s, bool pdl) {
     const int nj = rows_gemv_nj(p.K, p.m, dtype);
+    // bias, SiLU and the modulate prologue are served by the split-K kernel only
+    if (!nj && (p.bias || p.act || p.pro == PRO_LN_MOD)) return cudaErrorInvalidValue;
     if (nj) {
         if (dtype == 1) return p.m <= 1 ? launch_rows_nj<1, 1>(p, nj, num_sms, s, pdl)
                                         : launch_rows_nj<1, 2>(p, nj, num_sms, s, pdl);

@@ -149,13 +149,16 @@ struct RowsGemv {
         // The residual epilogue's operands of this thread's output (row tid / m, stream tid % m;
         // a segment has at most kRowsMaxRows * 2 <= kRowsThreads outputs), fetched together with
         // x rather than after the rows are summed.
-        float res_v = 0.f, ls_v = 0.f;
+        float res_v = 0.f, ls_v = 0.f, bias_v = 0.f;
         auto fetch_epi = [&](int seg) {
             const int srows = nrows - seg < kRowsMaxRows ? nrows - seg : kRowsMaxRows;
-            if (p.epi == EPI_RESID && tid < srows * m) {
+            if (tid < srows * m) {
                 const int row = row0 + seg + tid / m, mm = tid % m;
-                res_v = __ldcg(p.res + (size_t)mm * p.ldres + row);
-                if (p.ls) ls_v = p.ls[row];
+                if (p.bias) bias_v = p.bias[row];
+                if (p.epi == EPI_RESID) {
+                    res_v = __ldcg(p.res + (size_t)mm * p.ldres + row);
+                    if (p.ls) ls_v = __ldcg(p.ls + row);
+                }
             }
         };
         if (nrows > 0) fetch_epi(0);
@@ -199,12 +202,12 @@ struct RowsGemv {
 #pragma unroll
                     for (int e = 0; e < VEC / 2; ++e) {
                         const float2 v = xv[mm][j][e];
-                        part[mm] += (p.pro == PRO_LN) ? v.x + v.y : v.x * v.x + v.y * v.y;
+                        part[mm] += (p.pro != PRO_RMS) ? v.x + v.y : v.x * v.x + v.y * v.y;
                     }
             }
             block_sum(part, 0);  // mean (LayerNorm) or mean square (RMSNorm)
             float inv[MT], mean[MT];
-            if (p.pro == PRO_LN) {
+            if (p.pro != PRO_RMS) {
 #pragma unroll
                 for (int mm = 0; mm < MT; ++mm) {
                     mean[mm] = stat[mm];
@@ -234,14 +237,26 @@ struct RowsGemv {
                 const int k0 = gj[j] * VEC;
 #pragma unroll
                 for (int e = 0; e < VEC / 2; ++e) {
-                    const float2 w = *reinterpret_cast<const float2*>(p.nw + k0 + 2 * e);
+                    // a LayerNorm without affine weights (the flow head's final norm) is w 1, b 0
+                    const float2 w = p.nw ? *reinterpret_cast<const float2*>(p.nw + k0 + 2 * e)
+                                          : make_float2(1.f, 1.f);
                     float2 bb = make_float2(0.f, 0.f);
-                    if (p.pro == PRO_LN) bb = *reinterpret_cast<const float2*>(p.nb + k0 + 2 * e);
+                    if (p.pro != PRO_RMS && p.nb) bb = *reinterpret_cast<const float2*>(p.nb + k0 + 2 * e);
 #pragma unroll
                     for (int mm = 0; mm < MT; ++mm) {
                         float2& v = xv[mm][j][e];
                         v.x = (v.x - mean[mm]) * inv[mm] * w.x + bb.x;
                         v.y = (v.y - mean[mm]) * inv[mm] * w.y + bb.y;
+                    }
+                    if (p.pro == PRO_LN_MOD) {  // modulate: n (1 + scale) + shift
+                        const float2 sh = __ldcg(reinterpret_cast<const float2*>(p.mod + k0 + 2 * e));
+                        const float2 sc = __ldcg(reinterpret_cast<const float2*>(p.mod + K + k0 + 2 * e));
+#pragma unroll
+                        for (int mm = 0; mm < MT; ++mm) {
+                            float2& v = xv[mm][j][e];
+                            v.x = v.x * (1.0f + sc.x) + sh.x;
+                            v.y = v.y * (1.0f + sc.y) + sh.y;
+                        }
                     }
                 }
             }
@@ -327,6 +342,7 @@ struct RowsGemv {
                     const int r = tid / m, mm = tid - r * m;
                     float v = 0.f;
                     for (int w = 0; w < kRowsWarps; ++w) v += red[(w * kRowsMaxRows + r) * MT + mm];
+                    if (p.bias) v += bias_v;
                     const int row = rbase + r;
                     float out;
                     if (p.epi == EPI_RESID) {
@@ -336,7 +352,7 @@ struct RowsGemv {
                     } else if (p.epi == EPI_GELU) {
                         out = gelu_f(v);
                     } else {
-                        out = v;
+                        out = p.act == 1 ? silu_f(v) : v;
                     }
                     p.y[(size_t)mm * p.ldy + row] = out;
                 }

@@ -17,13 +17,20 @@ enum : unsigned {
 // GEMV: y[r][n] = sum_k W[n][k] * xin[r][k], W row-major [N][K], each weight read once for all
 // rows.  An optional norm prologue builds xin from x; an epilogue consumes the row sums.
 // ---------------------------------------------------------------------------------------------
-enum Prologue : int { PRO_NONE = 0, PRO_RMS = 1, PRO_LN = 2 };
+enum Prologue : int {
+    PRO_NONE = 0,
+    PRO_RMS = 1,
+    PRO_LN = 2,
+    PRO_LN_MOD = 3,  // LayerNorm (affine when nw / nb are set), then DiT's modulate:
+                     // xin = n * (1 + mod[K + k]) + mod[k]   (shift at mod[0..K), scale after)
+};
 enum Epilogue : int {
     EPI_STORE = 0,   // y[r][n] = v
     EPI_RESID = 1,   // y[r][n] = res[r][n] + (ls ? ls[n] * v : v)   (o-proj / down / MV_LS)
     EPI_SWIGLU = 2,  // rows interleaved (gate j, up j): y[r][j] = silu(v_2j) * v_2j+1
     EPI_GELU = 3,    // y[r][n] = 0.5 v (1 + erf(v / sqrt 2))
 };
+// Before any epilogue, v += bias[n] when bias is set; EPI_STORE then applies SiLU when act == 1.
 
 struct GemvParams {
     const void* W;
@@ -47,6 +54,9 @@ struct GemvParams {
     int unit;              // rows per partition unit (2 for SwiGLU pairs)
     int per_sm;            // split-K GEMV launch: CTAs per SM (0: 2).  One CTA per SM leaves room
                            // for the next kernel's CTAs to start and stage their loads early
+    const float* bias;     // [N] or null (split-K GEMV, m <= 2, only)
+    int act;               // EPI_STORE: 1 = SiLU
+    const float* mod;      // PRO_LN_MOD: [2K] shift then scale
 };
 
 // dtype: 0 f32, 1 bf16.  Launches with the programmatic-dependency attribute when pdl.

@@ -234,3 +234,52 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lens: torch.Ten
     L.check(lib.dec_attention(m, H, G, d, cap, _ptr(q), _ptr(k), _ptr(v), _ptr(lens), _ptr(out),
                               _ptr(workspace), workspace.numel(), _stream_handle(None)))
     return out
+
+
+# ----------------------------------------------------------------------------------------
+class FlowHead:
+    """The flow head (dec_flow_create .. dec_flow_destroy): one LSD step per call, conditioned
+    on a device row (the backbone's hidden state, read in place)."""
+
+    def __init__(self, shape, weights: Dict[str, np.ndarray], device="cuda",
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.lib = L.load()
+        self.shape = shape
+        dev = {k: to_device(v, device) for k, v in weights.items() if k not in ("cond", "noise")}
+        cfg = L.DecFlowConfig(dim=shape.dim, latent=shape.latent, cond=shape.cond,
+                              blocks=shape.blocks, ln_eps=shape.ln_eps, lsd_steps=1)
+        w = L.DecFlowWeights()
+        for n in ("ip_w", "ip_b", "cond_w", "cond_b", "t_const", "fada_w", "fada_b", "f_w", "f_b"):
+            setattr(w, n, _ptr(dev[n]))
+        self._arrays = []
+        for n in L.FLOW_BLOCK_FIELDS:
+            arr = (C.c_void_p * max(1, shape.blocks))(*[_ptr(dev[f"{n}{i}"])
+                                                        for i in range(shape.blocks)])
+            self._arrays.append(arr)
+            setattr(w, n, C.cast(arr, C.POINTER(C.c_void_p)))
+        h = C.c_void_p()
+        st = self.lib.dec_flow_create(C.byref(cfg), C.byref(w), _stream_handle(stream), C.byref(h))
+        L.check_flow(st, None)
+        self.h = h
+        del dev   # the head holds its own copy of the weights
+
+    def step(self, cond: torch.Tensor, noise: torch.Tensor,
+             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(noise)
+        L.check_flow(self.lib.dec_flow_step(self.h, _ptr(cond), _ptr(noise), _ptr(out)), self.h)
+        return out
+
+    def kernels_per_step(self) -> int:
+        return int(self.lib.dec_flow_kernels_per_step(self.h))
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            self.lib.dec_flow_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -267,5 +267,57 @@ SMALL_FLOWLM = dataclasses.replace(
     SMALL_CODEC, name="small_flowlm", seed=14, ring=40, window=40, max_pos=40, prefill=(7, 0),
     steps=30, layer_scale=False, head=True)
 
+# ----------------------------------------------------------------------------------------
+# the flow head (Pocket TTS on wgpu, PocketFlowGpu: SimpleMLPAdaLN, one LSD step)
+# ----------------------------------------------------------------------------------------
+@dataclass(frozen=True)
+class FlowShape:
+    name: str
+    dim: int          # the head's width
+    latent: int       # latent (noise) width
+    cond: int         # conditioning width: the backbone's d_model
+    blocks: int
+    seed: int
+    ln_eps: float = 1e-6
+
+
+# Widths the pages do not give; the conditioning is the FlowLM backbone's d_model (1024).
+FLOW_D512 = FlowShape(name="flow_d512_l32_b3", dim=512, latent=32, cond=1024, blocks=3, seed=6)
+SMALL_FLOW = FlowShape(name="small_flow", dim=136, latent=24, cond=256, blocks=2, seed=15)
+
+
+def generate_flow(f: FlowShape, calls: int = 4) -> Dict[str, np.ndarray]:
+    """Weights of the flow head, then `calls` conditioning rows and noise rows.
+
+    Draw order (PCG64 from the seed): input_proj W [dim][latent], b [dim]; cond W [dim][cond],
+    b [dim]; the time constant [dim]; per block: adaLN W [3 dim][dim], b [3 dim], in_ln w, b
+    [dim], m0 W [dim][dim], b [dim], m2 W [dim][dim], b [dim]; final adaLN W [2 dim][dim],
+    b [2 dim]; final W [latent][dim], b [latent]; then the inputs: cond [calls][cond] and noise
+    [calls][latent], N(0, 1).  Linear weights N(0, 1) x 0.02, biases and the time constant
+    N(0, 1) x 0.1, LayerNorm weights 1 + 0.01 N, biases 0.01 N.
+    """
+    r = np.random.Generator(np.random.PCG64(f.seed))
+    lin = lambda n, k: _normal(r, (n, k)) * np.float32(0.02)
+    vec = lambda n, s: _normal(r, (n,)) * np.float32(s)
+    d = {"ip_w": lin(f.dim, f.latent), "ip_b": vec(f.dim, 0.1),
+         "cond_w": lin(f.dim, f.cond), "cond_b": vec(f.dim, 0.1), "t_const": vec(f.dim, 0.1)}
+    for i in range(f.blocks):
+        d[f"ada_w{i}"] = lin(3 * f.dim, f.dim)
+        d[f"ada_b{i}"] = vec(3 * f.dim, 0.1)
+        d[f"ln_w{i}"] = np.float32(1.0) + vec(f.dim, 0.01)
+        d[f"ln_b{i}"] = vec(f.dim, 0.01)
+        d[f"m0_w{i}"] = lin(f.dim, f.dim)
+        d[f"m0_b{i}"] = vec(f.dim, 0.1)
+        d[f"m2_w{i}"] = lin(f.dim, f.dim)
+        d[f"m2_b{i}"] = vec(f.dim, 0.1)
+    d["fada_w"] = lin(2 * f.dim, f.dim)
+    d["fada_b"] = vec(2 * f.dim, 0.1)
+    d["f_w"] = lin(f.latent, f.dim)
+    d["f_b"] = vec(f.latent, 0.1)
+    d["cond"] = _normal(r, (calls, f.cond))
+    d["noise"] = _normal(r, (calls, f.latent))
+    return d
+
+
 SMALL: Dict[str, Workload] = {w.name: w for w in (SMALL_TALKER_F32, SMALL_TALKER_BF16,
                                                   SMALL_CODEC, SMALL_FLOWLM)}
