@@ -231,13 +231,14 @@ dec_status dec_truncate(dec_ctx* ctx, int stream, int new_len);
 
 /* Enqueue one stage of the step plan for rows 0..m-1, on the context's stream, from the
  * context's current buffers -- for timing a kernel on its own (the per-kernel attribution of
- * the pages' bench_steps, Mimi on wgpu).  stage: 0 norm + q/k/v GEMV, 1 attention (with its
+ * the pages' bench_steps, Mimi on wgpu).  chained != 0 launches the stage as a programmatic
+ * dependent of the previous kernel on the stream, as inside a step; 0 launches it alone.  stage: 0 norm + q/k/v GEMV, 1 attention (with its
  * prologue; two kernels: the split-K chunks, then the merge of their partials), 2 o-proj +
  * residual, 3 norm + gate/up + SwiGLU (codec: lin1 + GELU), 4 down + residual (codec: lin2);
  * every stage but 1 is exactly one kernel.  Layer 0's stages 0 and 2 read the context's internal input buffer.
  * Lengths do not advance; stage 1 writes the K/V row (ring slot) of the next position, which
  * the next step rewrites.  Not for use between a dec_step and its completion. */
-dec_status dec_launch_stage(dec_ctx* ctx, int layer, int stage, int m);
+dec_status dec_launch_stage(dec_ctx* ctx, int layer, int stage, int m, int chained);
 
 /* ---------------------------------------------------------------------------------------
  * The flow head (Pocket TTS on wgpu, PocketFlowGpu: SimpleMLPAdaLN, one LSD step), reading

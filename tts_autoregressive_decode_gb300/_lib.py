@@ -118,7 +118,7 @@ def load() -> C.CDLL:
         L.dec_read_tap.argtypes = [vp, i32, i32, vp]
         L.dec_kernels_per_step.argtypes = [vp, i32]
         L.dec_truncate.argtypes = [vp, i32, i32]
-        L.dec_launch_stage.argtypes = [vp, i32, i32, i32]
+        L.dec_launch_stage.argtypes = [vp, i32, i32, i32, i32]
         L.dec_gemv.argtypes = [i32, vp, i32, i32, vp, i32, vp, vp]
         L.dec_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.dec_attention_workspace_bytes.restype = sz

@@ -1026,7 +1026,7 @@ dec_status dec_truncate(dec_ctx* ctx, int stream, int new_len) {
     return DEC_OK;
 }
 
-dec_status dec_launch_stage(dec_ctx* ctx, int layer, int stage, int m) {
+dec_status dec_launch_stage(dec_ctx* ctx, int layer, int stage, int m, int chained) {
     if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");
     if (layer < 0 || layer >= ctx->cfg.layers || stage < 0 || stage > 4 || m < 1 || m > ctx->S)
         return fail(ctx, DEC_E_ARG, "bad layer, stage or m");
@@ -1036,7 +1036,7 @@ dec_status dec_launch_stage(dec_ctx* ctx, int layer, int stage, int m) {
             (ctx->cfg.kind == DEC_CODEC_WINDOWED && pos >= ctx->cfg.max_pos))
             return fail(ctx, DEC_E_CAPACITY, "stream %d is full", i);
     }
-    CUDA_TRY(ctx, launch_stage(ctx, layer, stage, m, ctx->io_in, ctx->stream, false),
+    CUDA_TRY(ctx, launch_stage(ctx, layer, stage, m, ctx->io_in, ctx->stream, chained != 0),
              "stage launch");
     return DEC_OK;
 }

@@ -183,8 +183,8 @@ class Decoder:
     def truncate(self, stream: int, new_len: int) -> None:
         L.check(self.lib.dec_truncate(self.h, stream, new_len), self.h)
 
-    def launch_stage(self, layer: int, stage: int, m: int) -> None:
-        L.check(self.lib.dec_launch_stage(self.h, layer, stage, m), self.h)
+    def launch_stage(self, layer: int, stage: int, m: int, chained: bool = False) -> None:
+        L.check(self.lib.dec_launch_stage(self.h, layer, stage, m, 1 if chained else 0), self.h)
 
     def close(self) -> None:
         if getattr(self, "h", None):
