@@ -46,7 +46,7 @@ NCU_TRAFFIC = {
     # gate/up GEMV (k_gemv_rows<bf16, m1, NJ1>, N = 12288, K = 2048): one launch captured with
     # ncu --set full on the 2-layer case of the same shapes (profiles/k_gemv_rows_gateup_*.md);
     # a launch does the same work at any layer count
-    W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_381_312, "source_sha": "df48366137bc5e9d"},
+    W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_382_336, "source_sha": "18ffb69f904e0f18"},
 }
 
 
@@ -104,9 +104,9 @@ def dominant_kernel(w: W.Workload, m: int):
     es = 2 if w.weight_dtype == "bf16" else 4
     h, I = w.hidden, w.inter
     if w.kind == "talker":
-        return (3, "norm + gate/up GEMV + SwiGLU (k_gemv)",
+        return (3, "norm + gate/up GEMV + SwiGLU (k_gemv_rows)",
                 2 * I * h * es + 4 * (m * h + h + m * I))
-    return (3, "LayerNorm + lin1 GEMV + GELU (k_gemv)", I * h * es + 4 * (m * h + 2 * h + m * I))
+    return (3, "LayerNorm + lin1 GEMV + GELU (k_gemv_rows)", I * h * es + 4 * (m * h + 2 * h + m * I))
 
 
 # the sources the gate/up GEMV (k_gemv_rows) is compiled from
@@ -507,7 +507,8 @@ def run_ours(args):
                                   "chained as programmatic dependents, as in the step"
                                   if k_alone_ms is not None else "the step's single launch"),
                      "alone_us_per_launch": k_alone_ms * 1e3 if k_alone_ms is not None else None,
-                     "peak_source": peak_src + " (burst: kernel timed alone)"},
+                     "peak_source": peak_src + (" (burst: the kernel's graph of one launch per layer, timed on its own)"
+                                                if k_alone_ms is not None else " (burst)")},
         "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                           "frac": step_gbs / peak, "bytes_per_step": nb},
         "gpu_launches": launches,
