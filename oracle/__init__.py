@@ -70,6 +70,10 @@ def lib(precision: str = "f32") -> C.CDLL:
         L.orc_prefill_kv.argtypes = [C.c_void_p, C.c_int, _fp, _fp, C.c_int]
         L.orc_step.argtypes = [C.c_void_p, C.c_int, _fp, C.POINTER(C.c_int), _dp, _dp]
         L.orc_prefill.argtypes = [C.c_void_p, C.c_int, C.c_int, _fp, _dp]
+        _ip = C.POINTER(C.c_int)
+        L.orc_set_mrope.argtypes = [C.c_void_p, _ip]
+        L.orc_step_mrope.argtypes = [C.c_void_p, C.c_int, _fp, _ip, _ip, _dp, _dp]
+        L.orc_prefill_mrope.argtypes = [C.c_void_p, C.c_int, C.c_int, _fp, _ip, _dp]
         L.orc_flow_step.argtypes = [C.c_void_p, _fp, _fp, _dp]
         L.orc_set_head.argtypes = [C.c_void_p, _fp, _fp, _fp]
         L.orc_eos.argtypes = [C.c_void_p, C.c_int]
@@ -315,25 +319,46 @@ class OracleModel:
         if rc != 0:
             raise ValueError(f"orc_prefill_kv failed ({rc})")
 
-    def step(self, x_in: np.ndarray, pos: Sequence[int], taps: bool = False):
+    def set_mrope(self, assign: Optional[Sequence[int]]) -> None:
+        """Talker: the axis (0 t, 1 h, 2 w) of each of the head_dim/2 rope frequencies, or None
+        for the 1-D rope."""
+        a = None if assign is None else np.ascontiguousarray(assign, dtype=np.int32)
+        if a is not None:
+            if a.shape != (self.w.head_dim // 2,):
+                raise ValueError("the axis map needs head_dim/2 entries")
+            self._keep.append(a)
+        if self.L.orc_set_mrope(self.h, _ptr(a, C.c_int) if a is not None else None):
+            raise ValueError("oracle rejected the axis map")
+
+    def step(self, x_in: np.ndarray, pos: Sequence[int], taps: bool = False, rope_pos=None):
+        """One step; rope_pos [rows][3] (optional): the rows' t, h, w rotary positions."""
         x_in = np.ascontiguousarray(x_in, dtype=np.float32)
         rows = x_in.shape[0]
         p = np.ascontiguousarray(pos, dtype=np.int32)
+        r3 = None if rope_pos is None else np.ascontiguousarray(rope_pos, dtype=np.int32)
+        if r3 is not None and r3.shape != (rows, 3):
+            raise ValueError("rope_pos must be [rows][3]")
         out = np.empty((rows, self.w.hidden), np.float64)
         t = np.empty((self.w.layers, rows, self.w.hidden), np.float64) if taps else None
-        rc = self.L.orc_step(self.h, rows, _ptr(x_in, C.c_float), _ptr(p, C.c_int),
-                             _ptr(out, C.c_double), _ptr(t, C.c_double) if taps else None)
+        rc = self.L.orc_step_mrope(self.h, rows, _ptr(x_in, C.c_float), _ptr(p, C.c_int),
+                                   _ptr(r3, C.c_int) if r3 is not None else None,
+                                   _ptr(out, C.c_double), _ptr(t, C.c_double) if taps else None)
         if rc != 0:
             raise ValueError(f"orc_step failed ({rc})")
         return (out, t) if taps else out
 
-    def prefill(self, stream: int, x_in: np.ndarray) -> np.ndarray:
+    def prefill(self, stream: int, x_in: np.ndarray, rope_pos=None) -> np.ndarray:
         """Causal prefill of the rows of x_in [n][hidden] into `stream`: every position's
-        final-norm hidden [n][hidden]."""
+        final-norm hidden [n][hidden].  rope_pos [n][3] (optional): per-axis rotary positions."""
         x_in = np.ascontiguousarray(x_in, dtype=np.float32)
         n = x_in.shape[0]
+        r3 = None if rope_pos is None else np.ascontiguousarray(rope_pos, dtype=np.int32)
+        if r3 is not None and r3.shape != (n, 3):
+            raise ValueError("rope_pos must be [n][3]")
         out = np.empty((n, self.w.hidden), np.float64)
-        rc = self.L.orc_prefill(self.h, stream, n, _ptr(x_in, C.c_float), _ptr(out, C.c_double))
+        rc = self.L.orc_prefill_mrope(self.h, stream, n, _ptr(x_in, C.c_float),
+                                      _ptr(r3, C.c_int) if r3 is not None else None,
+                                      _ptr(out, C.c_double))
         if rc != 0:
             raise ValueError(f"orc_prefill failed ({rc})")
         return out

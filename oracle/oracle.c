@@ -28,6 +28,10 @@
  *                     LN, lin1, GELU, lin2 + LS; the output is the residual stream
  *
  * Readings where the pages are silent (each is listed with its reason in the design notes):
+ *   - multimodal rope (the talker's "interleaved MRoPE"): frequency i of the rotate_half table
+ *     turns by the position of one of three axes (t, h, w), named by a per-frequency axis map
+ *     the caller supplies (the pages give no section split); equal positions on all axes give
+ *     the 1-D table (the pages' MRoPE-uniform identity)
  *   - rope tables: angle pos * theta^(-2i/d), cos/sin computed in double, rounded to orc_real
  *     (the talker's table builder is not printed; the codec computes the same angle in-kernel)
  *   - codec rope base 10000 (the value in rope_push_src)
@@ -114,6 +118,18 @@ static void rope_table_r(int d, double theta, int pos, real* c, real* s) {
     for (int i = 0; i < d / 2; ++i) {
         double inv_freq = pow(theta, -2.0 * (double)i / (double)d);
         double ang = (double)pos * inv_freq;
+        c[i] = (real)cos(ang);
+        s[i] = (real)sin(ang);
+    }
+}
+
+/* the multimodal table: angle(i) = pos3[axis(i)] * theta^(-2i/d), axis(i) = assign[i]
+ * (assign NULL: every frequency follows axis 0) */
+static void mrope_table_r(int d, double theta, const int* pos3, const int* assign, real* c,
+                          real* s) {
+    for (int i = 0; i < d / 2; ++i) {
+        double inv_freq = pow(theta, -2.0 * (double)i / (double)d);
+        double ang = (double)pos3[assign ? assign[i] : 0] * inv_freq;
         c[i] = (real)cos(ang);
         s[i] = (real)sin(ang);
     }
@@ -280,12 +296,10 @@ void orc_rope_table(int d, double theta, int pos, double* c, double* s) {
 
 void orc_mrope_table(int d, double theta, const int* pos3, const int* assign, double* c,
                      double* s) {
-    for (int i = 0; i < d / 2; ++i) {
-        double inv_freq = pow(theta, -2.0 * (double)i / (double)d);
-        double ang = (double)pos3[assign[i]] * inv_freq;
-        c[i] = (double)(real)cos(ang);
-        s[i] = (double)(real)sin(ang);
-    }
+    real cr[256], sr[256];
+    mrope_table_r(d, theta, pos3, assign, cr, sr);
+    from_real(cr, d / 2, c);
+    from_real(sr, d / 2, s);
 }
 
 void orc_rope_rotate_half(double* x, int d, const double* c, const double* s) {
@@ -362,6 +376,7 @@ struct orc_model {
     real* vc;
     uint32_t* pr;   /* codec: [layers][streams][ring] position stamps */
     int* len;       /* [streams] */
+    int* rope_assign; /* talker: [head_dim/2] axis of each rope frequency, or NULL (axis 0) */
 };
 
 static size_t kv_index(const orc_model* m, int layer, int stream, int slot) {
@@ -408,6 +423,7 @@ void orc_destroy(orc_model* m) {
     free(m->kc);
     free(m->vc);
     free(m->pr);
+    free(m->rope_assign);
     free(m->len);
     free(m->eos);
     free(m);
@@ -483,8 +499,10 @@ int orc_read_kv(const orc_model* m, int layer, int stream, int pos, double* k, d
     return 0;
 }
 
-/* one talker layer for one stream, in build_step_plan's order */
-static void talker_layer(orc_model* m, int l, int s, int pos, real* x, real* buf) {
+/* one talker layer for one stream, in build_step_plan's order; the new K/V row goes to cache
+ * row pos, and the rope turns by pos or, with pos3, by the per-axis positions pos3[0..2] */
+static void talker_layer(orc_model* m, int l, int s, int pos, const int* pos3, real* x,
+                         real* buf) {
     const orc_config* c = &m->c;
     const orc_layer* W = &m->layers[l];
     int h = c->hidden, d = c->head_dim, H = c->q_heads, G = c->kv_heads, ni = c->inter;
@@ -510,7 +528,10 @@ static void talker_layer(orc_model* m, int l, int s, int pos, real* x, real* buf
     matvec_r(W->wv, bf, kvw, h, n, v);
     for (int hh = 0; hh < H; ++hh) rms_norm_r(q + hh * d, W->q_norm, d, eps, q + hh * d);
     for (int gg = 0; gg < G; ++gg) rms_norm_r(k + gg * d, W->k_norm, d, eps, k + gg * d);
-    rope_table_r(d, c->rope_theta, pos, cs, sn);
+    if (pos3)
+        mrope_table_r(d, c->rope_theta, pos3, m->rope_assign, cs, sn);
+    else
+        rope_table_r(d, c->rope_theta, pos, cs, sn);
     for (int hh = 0; hh < H; ++hh) rope_rotate_half_r(q + hh * d, d, cs, sn);
     for (int gg = 0; gg < G; ++gg) rope_rotate_half_r(k + gg * d, d, cs, sn);
     real* kd = m->kc + kv_index(m, l, s, pos);
@@ -580,13 +601,41 @@ static void codec_layer(orc_model* m, int l, int s, int pos, real* x, real* buf)
     for (int i = 0; i < D; ++i) x[i] = x[i] + (W->ls2 ? (real)W->ls2[i] * y[i] : y[i]);
 }
 
+static int pos3_ok(const orc_model* m, const int* p3) {
+    for (int a = 0; a < 3; ++a)
+        if (p3[a] < 0 || p3[a] >= m->c.max_pos) return 0;
+    return 1;
+}
+
+int orc_set_mrope(orc_model* m, const int* assign) {
+    if (!m || m->c.kind != ORC_TALKER) return -1;
+    const int half = m->c.head_dim / 2;
+    if (assign)
+        for (int i = 0; i < half; ++i)
+            if (assign[i] < 0 || assign[i] > 2) return -1;
+    free(m->rope_assign);
+    m->rope_assign = NULL;
+    if (assign) {
+        m->rope_assign = (int*)malloc(sizeof(int) * (size_t)half);
+        memcpy(m->rope_assign, assign, sizeof(int) * (size_t)half);
+    }
+    return 0;
+}
+
 int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* out,
              double* taps) {
+    return orc_step_mrope(m, rows, x_in, pos, NULL, out, taps);
+}
+
+int orc_step_mrope(orc_model* m, int rows, const float* x_in, const int* pos, const int* pos3,
+                   double* out, double* taps) {
     if (!m || rows < 1 || rows > m->c.streams || !x_in || !pos || !out) return -1;
     const orc_config* c = &m->c;
+    if (pos3 && c->kind != ORC_TALKER) return -4;
     for (int s = 0; s < rows; ++s) {
         if (pos[s] != m->len[s]) return -2;
         if (pos[s] >= c->max_pos) return -3;
+        if (pos3 && !pos3_ok(m, pos3 + 3 * s)) return -3;
     }
     int h = c->hidden;
     size_t nbuf = (size_t)8 * h + 4 * (size_t)c->q_heads * c->head_dim +
@@ -598,7 +647,7 @@ int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* 
         for (int i = 0; i < h; ++i) x[i] = (real)x_in[(size_t)s * h + i];
         for (int l = 0; l < c->layers; ++l) {
             if (c->kind == ORC_TALKER)
-                talker_layer(m, l, s, pos[s], x, buf);
+                talker_layer(m, l, s, pos[s], pos3 ? pos3 + 3 * s : NULL, x, buf);
             else
                 codec_layer(m, l, s, pos[s], x, buf);
             if (taps) from_real(x, h, taps + ((size_t)l * rows + s) * h);
@@ -675,10 +724,18 @@ int orc_flow_step(const orc_flow* f, const float* cond, const float* noise, doub
 }
 
 int orc_prefill(orc_model* m, int stream, int n, const float* x_in, double* out) {
+    return orc_prefill_mrope(m, stream, n, x_in, NULL, out);
+}
+
+int orc_prefill_mrope(orc_model* m, int stream, int n, const float* x_in, const int* pos3,
+                      double* out) {
     if (!m || stream < 0 || stream >= m->c.streams || n < 1 || !x_in || !out) return -1;
     const orc_config* c = &m->c;
     if (c->kind != ORC_TALKER) return -4;
     if (m->len[stream] + n > c->max_pos) return -3;
+    if (pos3)
+        for (int r = 0; r < n; ++r)
+            if (!pos3_ok(m, pos3 + 3 * r)) return -3;
     const int h = c->hidden;
     size_t nbuf = (size_t)8 * h + 4 * (size_t)c->q_heads * c->head_dim +
                   4 * (size_t)c->inter + (size_t)c->head_dim + 2 * (size_t)m->slots + 64;
@@ -688,7 +745,8 @@ int orc_prefill(orc_model* m, int stream, int n, const float* x_in, double* out)
     for (int r = 0; r < n; ++r) {  /* row r: one step at position len + r */
         const int pos = m->len[stream];
         for (int i = 0; i < h; ++i) x[i] = (real)x_in[(size_t)r * h + i];
-        for (int l = 0; l < c->layers; ++l) talker_layer(m, l, stream, pos, x, buf);
+        for (int l = 0; l < c->layers; ++l)
+            talker_layer(m, l, stream, pos, pos3 ? pos3 + 3 * r : NULL, x, buf);
         rms_norm_r(x, m->final_norm, h, (real)c->norm_eps, y);
         from_real(y, h, out + (size_t)r * h);
         m->len[stream] += 1;

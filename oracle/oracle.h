@@ -111,6 +111,16 @@ int orc_prefill_kv(orc_model* m, int stream, const float* k, const float* v, int
  * the residual stream after each layer.  Returns 0 or a negative error code. */
 int orc_step(orc_model* m, int rows, const float* x_in, const int* pos, double* out, double* taps);
 
+/* Talker multimodal rope (Qwen3-TTS talker on wgpu, module notes: "interleaved MRoPE"; uniform
+ * positions reduce it to the 1-D rope).  assign [head_dim/2]: the axis (0 t, 1 h, 2 w) whose
+ * position turns rope frequency i; NULL restores the 1-D rope.  Returns 0, or -1 (codec, an
+ * entry outside 0..2). */
+int orc_set_mrope(orc_model* m, const int* assign);
+/* orc_step with per-axis rotary positions pos3 [rows][3] (each in 0..max_pos-1; NULL: the 1-D
+ * rope at pos).  The K/V row still goes to cache row pos[i].  -4 for a codec model. */
+int orc_step_mrope(orc_model* m, int rows, const float* x_in, const int* pos, const int* pos3,
+                   double* out, double* taps);
+
 /* Codec only: the FlowLM backbone's head (Pocket TTS on wgpu, PocketBackboneGpu): after the
  * stack, out = LayerNorm(x; norm_w, norm_b) is the step's output instead of x, and with eos_w
  * the EOS logit eos_w . out (ascending sum; its bias is added by the caller, as the page does on
@@ -126,6 +136,9 @@ double orc_eos(const orc_model* m, int stream);
  * a causal mask gives row r.  x_in [n][hidden], out [n][hidden].  Talker only.
  * Returns 0, or < 0 on a bad argument or capacity. */
 int orc_prefill(orc_model* m, int stream, int n, const float* x_in, double* out);
+/* orc_prefill with per-axis rotary positions pos3 [n][3] for the rows (NULL: 1-D rope). */
+int orc_prefill_mrope(orc_model* m, int stream, int n, const float* x_in, const int* pos3,
+                      double* out);
 void orc_reset(orc_model* m, int stream);
 
 /* ---- the flow head (Pocket TTS on wgpu, PocketFlowGpu: SimpleMLPAdaLN, one LSD step) ---- */

@@ -40,7 +40,16 @@ MUTATIONS = [
      "memcpy(y, x, sizeof(real) * (size_t)h);"),
     ("kv_append_wrong_row", "real* kd = m->kc + kv_index(m, l, s, pos);",
      "real* kd = m->kc + kv_index(m, l, s, pos > 0 ? pos - 1 : 0);"),
+    ("mrope_axis_shifted", "(double)pos3[assign ? assign[i] : 0]",
+     "(double)pos3[assign ? (assign[i] + 1) % 3 : 0]"),
+    ("mrope_keys_turned_by_cache_position",
+     "for (int gg = 0; gg < G; ++gg) rope_rotate_half_r(k + gg * d, d, cs, sn);",
+     "rope_table_r(d, c->rope_theta, pos, cs, sn);\n"
+     "    for (int gg = 0; gg < G; ++gg) rope_rotate_half_r(k + gg * d, d, cs, sn);"),
+    ("mrope_rows_share_row0_positions", "pos3 ? pos3 + 3 * s : NULL", "pos3 ? pos3 : NULL"),
 ]
+
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_mrope.py"]
 
 
 @pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
@@ -52,8 +61,8 @@ def test_pins_catch_planted_mistake(name, old, new):
         open(mut, "w").write(src.replace(old, new))
         obuild.build(force=True, src=mut, out_dir=tmp)
         env = dict(os.environ, ORACLE_LIB_DIR=tmp)
-        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                            os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] +
+                           [os.path.join(ROOT, "tests", f) for f in PIN_FILES],
                            cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
         assert r.returncode != 0, f"pins did not catch mutation {name}:\n{r.stdout[-2000:]}"
 
@@ -63,7 +72,7 @@ def test_control_unmutated_copy_passes_the_pins():
     with tempfile.TemporaryDirectory() as tmp:
         obuild.build(force=True, src=obuild.SRC, out_dir=tmp)
         env = dict(os.environ, ORACLE_LIB_DIR=tmp)
-        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                            os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] +
+                           [os.path.join(ROOT, "tests", f) for f in PIN_FILES],
                            cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
         assert r.returncode == 0, r.stdout[-3000:]
