@@ -185,6 +185,32 @@ int dec_prefill_block_rows(const dec_ctx* ctx);
  * an error. */
 dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, float* hidden_out);
 
+/* Multimodal rope of the talker (Qwen3-TTS talker on wgpu, module notes: the talker's rope is
+ * interleaved MRoPE; with equal positions on its three axes it is the 1-D rope the tables hold).
+ * axis_host HOST [n], n = head_dim / 2: the axis (0 t, 1 h, 2 w) whose rotary position turns
+ * rope frequency i; the pages give no section split, so the caller supplies the map (an
+ * interleaved split puts h on i = 1, 4, 7, ... and w on i = 2, 5, 8, ... up to their sections).
+ * NULL sets every frequency to axis t.  The map is used only by the steps and prefills given
+ * per-axis rotary positions (dec_step_mrope, dec_prefill_mrope).  Synchronous (waits for the
+ * context's stream).  Errors: DEC_E_ARG (n, an entry outside 0..2), DEC_E_UNSUPPORTED (codec). */
+dec_status dec_set_mrope(dec_ctx* ctx, const int32_t* axis_host, int n);
+
+/* dec_step with per-axis rotary positions (talker).
+ *   rope_pos  DEVICE [m][3] int32 (4-byte aligned): row i's t, h, w rotary positions, each in
+ *             0..max_pos-1; NULL is dec_step.  The K/V row still goes to cache row pos[i].
+ * The buffer is read when the step runs (like x_in), so it may be rewritten between steps; its
+ * pointer is part of the captured graph's key.  Steps with rope_pos always run the multi-kernel
+ * plan (6 * layers + 1 kernels, also with DEC_FLAG_PERSISTENT).  A position outside 0..max_pos-1
+ * leaves that row's attention undone and is reported as DEC_E_DEVICE_CHECK by the next dec_sync.
+ * Errors as dec_step, plus DEC_E_ARG (alignment) and DEC_E_UNSUPPORTED (codec with rope_pos). */
+dec_status dec_step_mrope(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos,
+                          const int32_t* rope_pos, float* hidden_out);
+
+/* dec_prefill with per-axis rotary positions: rope_pos DEVICE [n][3] int32, row r's t, h, w
+ * positions (NULL is dec_prefill); the rows still go to cache rows len .. len + n - 1. */
+dec_status dec_prefill_mrope(dec_ctx* ctx, int stream, int n, const float* x,
+                             const int32_t* rope_pos, float* out);
+
 /* dec_step with HOST buffers, blocking, as the talker page's step() returns its hidden state
  * to the host (Qwen3-TTS talker on wgpu, step(): write_buffer, submit, blocking read).
  * x_in_host [m][hidden] and hidden_out_host [m][hidden] f32 in host memory (pinned or not);
@@ -232,7 +258,8 @@ dec_status dec_truncate(dec_ctx* ctx, int stream, int new_len);
 /* Enqueue one stage of the step plan for rows 0..m-1, on the context's stream, from the
  * context's current buffers -- for timing a kernel on its own (the per-kernel attribution of
  * the pages' bench_steps, Mimi on wgpu).  chained != 0 launches the stage as a programmatic
- * dependent of the previous kernel on the stream, as inside a step; 0 launches it alone.  stage: 0 norm + q/k/v GEMV, 1 attention (with its
+ * dependent of the previous kernel on the stream, as inside a step; 0 launches it alone.
+ * stage: 0 norm + q/k/v GEMV, 1 attention (with its
  * prologue; two kernels: the split-K chunks, then the merge of their partials), 2 o-proj +
  * residual, 3 norm + gate/up + SwiGLU (codec: lin1 + GELU), 4 down + residual (codec: lin2);
  * every stage but 1 is exactly one kernel.  Layer 0's stages 0 and 2 read the context's internal input buffer.

@@ -76,7 +76,22 @@ def test_null_arguments(lib):
     assert lib.dec_reset(None, 0) == L.DEC_E_ARG
     assert lib.dec_sync(None) == L.DEC_E_ARG
     assert lib.dec_get_len(None, 0) == -1
+    assert lib.dec_set_mrope(None, None, 0) == L.DEC_E_ARG
+    assert lib.dec_step_mrope(None, 1, None, None, None, None) == L.DEC_E_ARG
+    assert lib.dec_prefill_mrope(None, 0, 1, None, None, None) == L.DEC_E_ARG
     lib.dec_destroy(None)
+
+
+def test_mrope_axis_maps_from_sections():
+    from tts_autoregressive_decode_gb300.decoder import mrope_axes
+    a = mrope_axes(128, (24, 20, 20))
+    assert [a.count(k) for k in range(3)] == [24, 20, 20]
+    assert a[:7] == [0, 1, 2, 0, 1, 2, 0] and a[58:] == [1, 2, 0, 0, 0, 0]
+    assert mrope_axes(128, (16, 24, 24), interleaved=False) == [0] * 16 + [1] * 24 + [2] * 24
+    assert mrope_axes(64, (32, 0, 0)) == [0] * 32
+    for bad in ((20, 20, 20), (10, 27, 27), (-1, 33, 32)):
+        with pytest.raises(ValueError):
+            mrope_axes(128, bad)
 
 
 def test_stateless_entries_validate_before_launch(lib):

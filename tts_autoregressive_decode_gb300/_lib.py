@@ -21,7 +21,8 @@ DEC_FLAG_TAPS, DEC_FLAG_NO_GRAPH, DEC_FLAG_PERSISTENT = 1, 2, 4
 
 # every symbol include/dec.h declares
 EXPORTS = ("dec_create", "dec_destroy", "dec_last_error", "dec_set_stream", "dec_prefill_kv",
-           "dec_prefill", "dec_prefill_block_rows", "dec_read_eos", "dec_step", "dec_step_host", "dec_reset", "dec_sync", "dec_get_len", "dec_read_kv",
+           "dec_prefill", "dec_prefill_block_rows", "dec_read_eos", "dec_step", "dec_step_host",
+           "dec_set_mrope", "dec_step_mrope", "dec_prefill_mrope", "dec_reset", "dec_sync", "dec_get_len", "dec_read_kv",
            "dec_read_tap", "dec_kernels_per_step", "dec_truncate", "dec_launch_stage",
            "dec_gemv", "dec_attention_workspace_bytes", "dec_attention",
            "dec_attention_noalloc", "dec_flow_create", "dec_flow_step", "dec_flow_destroy",
@@ -110,6 +111,9 @@ def load() -> C.CDLL:
         L.dec_flow_kernels_per_step.restype = i32
         L.dec_prefill_block_rows.restype = i32
         L.dec_step.argtypes = [vp, i32, vp, C.POINTER(C.c_int32), vp]
+        L.dec_set_mrope.argtypes = [vp, C.POINTER(C.c_int32), i32]
+        L.dec_step_mrope.argtypes = [vp, i32, vp, C.POINTER(C.c_int32), vp, vp]
+        L.dec_prefill_mrope.argtypes = [vp, i32, i32, vp, vp, vp]
         L.dec_step_host.argtypes = [vp, i32, vp, C.POINTER(C.c_int32), vp]
         L.dec_reset.argtypes = [vp, i32]
         L.dec_sync.argtypes = [vp]
@@ -127,7 +131,8 @@ def load() -> C.CDLL:
         for f in ("dec_set_stream", "dec_prefill_kv", "dec_step", "dec_step_host", "dec_reset",
                   "dec_sync", "dec_read_kv", "dec_read_tap", "dec_gemv", "dec_attention",
                   "dec_attention_noalloc",
-                  "dec_truncate", "dec_launch_stage", "dec_prefill", "dec_read_eos"):
+                  "dec_truncate", "dec_launch_stage", "dec_prefill", "dec_read_eos",
+                  "dec_set_mrope", "dec_step_mrope", "dec_prefill_mrope"):
             getattr(L, f).restype = i32
         L.dec_get_len.restype = i32
         L.dec_kernels_per_step.restype = i32

@@ -149,14 +149,13 @@ __global__ void __launch_bounds__(kAppendWarps * 32) k_prefill_append(const Attn
     const int idx = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
     if (idx >= p.m * p.G) return;
     const int r = idx / p.G, g = idx - r * p.G;
-    const int base = __ldcg(p.len + p.stream);
-    const int pos = base + r;
-    if (base < 0 || pos >= p.max_pos || pos >= p.slots) {
+    const ChunkInfo ci = chunk_info(p, r, 0);  // position len + r and its rotary positions
+    if (ci.bad) {
         if (lane == 0) flag_check(p.status, CHECK_BOUNDS);
         return;
     }
-    const size_t row = (((size_t)p.stream * p.G + g) * p.slots + pos) * D;
-    talker_new_kv<D>(p, r, g, pos, lane, p.kc + row, p.vc + row);
+    const size_t row = (((size_t)p.stream * p.G + g) * p.slots + ci.pos) * D;
+    talker_new_kv<D>(p, r, g, ci, lane, p.kc + row, p.vc + row);
 }
 
 template <int D>

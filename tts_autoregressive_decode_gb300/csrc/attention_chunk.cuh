@@ -112,6 +112,8 @@ struct ChunkInfo {
     int nk;       // keys in the chunk
     int ncached;  // rows to stage from the cache
     int newrow;   // row of the chunk that receives the new k/v (-1: none)
+    int rt, rh, rw; // TALKER/PREFILL: the rotary positions of the t, h, w axes (all pos
+                    // without per-axis positions)
     bool bad;     // position / length out of range: the item does nothing
 };
 
@@ -153,7 +155,30 @@ __device__ __forceinline__ ChunkInfo chunk_info(const AttnParams& p, int r, int 
         if (slot >= ci.k0 && slot < ci.k0 + CH) ci.newrow = slot - ci.k0;
         ci.bad = ci.pos < 0 || ci.pos >= p.max_pos;
     }
+    ci.rt = ci.rh = ci.rw = ci.pos;
+    if (p.rope_pos && (p.mode == ATTN_TALKER || p.mode == ATTN_PREFILL)) {
+        const int32_t* q3 = p.rope_pos + 3 * (size_t)r;
+        ci.rt = __ldcg(q3);
+        ci.rh = __ldcg(q3 + 1);
+        ci.rw = __ldcg(q3 + 2);
+        const int lo = min(ci.rt, min(ci.rh, ci.rw)), hi = max(ci.rt, max(ci.rh, ci.rw));
+        if (lo < 0 || hi >= p.max_pos) ci.bad = true;
+    }
     return ci;
+}
+
+// cos and sin of rotate_half rope frequency f for a row: from the table row of its cache
+// position or, with per-axis rotary positions, of the position of the axis frequency f follows.
+template <int HALF>
+__device__ __forceinline__ void rope_cs(const AttnParams& p, const ChunkInfo& ci, int f, float& c,
+                                        float& s) {
+    int pf = ci.pos;
+    if (p.rope_pos) {
+        const int a = __ldg(p.rope_axis + f);
+        pf = a == 1 ? ci.rh : (a == 2 ? ci.rw : ci.rt);
+    }
+    c = p.rope_cos[(size_t)pf * HALF + f];
+    s = p.rope_sin[(size_t)pf * HALF + f];
 }
 
 // Thread 0 only: arm the mbarrier for the item's staged rows and start the two bulk copies.
@@ -194,11 +219,12 @@ __device__ __forceinline__ float butterfly8_keys(const float v[8], int lane) {
 }
 
 // The talker's new key and value of kv head g from raw q/k/v row `row` (per-head RMSNorm of k
-// with the shared [d] weight, rotate_half rope at `pos`; v as is), by one warp: element
-// t = lane + 32 j of the results is written to k_out[t] and v_out[t].
+// with the shared [d] weight, rotate_half rope at the row's positions `ci`; v as is), by one
+// warp: element t = lane + 32 j of the results is written to k_out[t] and v_out[t].
 template <int D>
-__device__ __forceinline__ void talker_new_kv(const AttnParams& p, int row, int g, int pos,
-                                              int lane, float* k_out, float* v_out) {
+__device__ __forceinline__ void talker_new_kv(const AttnParams& p, int row, int g,
+                                              const ChunkInfo& ci, int lane, float* k_out,
+                                              float* v_out) {
     constexpr int HALF = D / 2;
     const float* ksrc = p.qkv + (size_t)row * p.ldqkv + (size_t)p.H * D + (size_t)g * D;
     const float* vsrc = ksrc + (size_t)p.G * D;
@@ -213,15 +239,15 @@ __device__ __forceinline__ void talker_new_kv(const AttnParams& p, int row, int 
     const float inv = 1.0f / sqrtf(ss / (float)D + p.eps);
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) v[j] = v[j] * inv * p.kn[lane + 32 * j];
-    const float* cs = p.rope_cos + (size_t)pos * HALF;
-    const float* sn = p.rope_sin + (size_t)pos * HALF;
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
         const int t = lane + 32 * j;
         const int jj = (j + D / 64) % (D / 32);  // element t +- D/2, same lane
         const float rot = (t < HALF) ? -v[jj] : v[jj];
         const int f = t < HALF ? t : t - HALF;
-        k_out[t] = v[j] * cs[f] + rot * sn[f];
+        float c, s;
+        rope_cs<HALF>(p, ci, f, c, s);
+        k_out[t] = v[j] * c + rot * s;
         v_out[t] = __ldcg(vsrc + t);
     }
 }
@@ -268,15 +294,15 @@ __device__ bool chunk_compute(const AttnParams& p, int r, int g, int c, const Ch
             const float inv = 1.0f / sqrtf(ss / (float)D + p.eps);
 #pragma unroll
             for (int j = 0; j < D / 32; ++j) v[j] = v[j] * inv * p.qn[lane + 32 * j];
-            const float* cs = p.rope_cos + (size_t)pos * HALF;
-            const float* sn = p.rope_sin + (size_t)pos * HALF;
 #pragma unroll
             for (int j = 0; j < D / 32; ++j) {
                 const int t = lane + 32 * j;
                 const int jj = (j + D / 64) % (D / 32);       // element t +- D/2, same lane
                 const float rot = (t < HALF) ? -v[jj] : v[jj];
                 const int f = t < HALF ? t : t - HALF;
-                qs[i * D + t] = v[j] * cs[f] + rot * sn[f];
+                float c, s;
+                rope_cs<HALF>(p, ci, f, c, s);
+                qs[i * D + t] = v[j] * c + rot * s;
             }
         } else {
             const float* src = p.qkv + (size_t)r * p.ldqkv + (size_t)hq * D;
@@ -292,7 +318,7 @@ __device__ bool chunk_compute(const AttnParams& p, int r, int g, int c, const Ch
     if (newrow >= 0 && warp == (group % kChunkWarps)) {
         // the new key and value of kv head g at position pos
         if (mode == ATTN_TALKER) {
-            talker_new_kv<D>(p, r, g, pos, lane, sm.knew, sm.vnew);
+            talker_new_kv<D>(p, r, g, ci, lane, sm.knew, sm.vnew);
         } else {
             const int D_model = p.H * D;
             const float* ksrc = p.qkv + (size_t)r * p.ldqkv + D_model + (size_t)g * D;

@@ -51,6 +51,7 @@ struct PlanEntry {
     int m;
     const float* x_in;
     float* out;
+    const int32_t* rope;     // per-axis rotary positions of the rows (multi-kernel plans), or null
     StepPhase* phases;       // device, or null (multi-kernel plan)
     cudaGraphExec_t exec;
     cudaGraph_t graph;       // persistent plan: the captured graph, owner of `node`
@@ -114,6 +115,7 @@ struct dec_ctx {
     float *kc = nullptr, *vc = nullptr;
     uint32_t* pr = nullptr;
     float *rope_cos = nullptr, *rope_sin = nullptr;
+    int32_t* rope_axis = nullptr;  // [d/2] multimodal rope: the axis of each frequency
     float *xres = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr;
     float *part = nullptr, *part_ml = nullptr;  // attention chunk partials
     int32_t* len_dev = nullptr;
@@ -229,7 +231,7 @@ void destroy_plans(dec_ctx* ctx) {
 // Parameters of stage `stage` of layer `l` for rows 0..m-1 (see dec_launch_stage for the
 // stages): a GEMV (returns false) or, for stage 1, the attention (returns true; `a` is filled).
 bool stage_params(dec_ctx* ctx, int l, int stage, int m, const float* x_in, GemvParams& g,
-                  AttnParams& a) {
+                  AttnParams& a, const int32_t* rope_pos = nullptr) {
     const dec_config& c = ctx->cfg;
     const bool talker = c.kind == DEC_QWEN3_TALKER;
     const int h = c.hidden, d = c.head_dim, H = c.q_heads, G = c.kv_heads, I = c.inter;
@@ -278,6 +280,8 @@ bool stage_params(dec_ctx* ctx, int l, int stage, int m, const float* x_in, Gemv
             a.rope_cos = ctx->rope_cos;
             a.rope_sin = ctx->rope_sin;
             a.max_pos = c.max_pos;
+            a.rope_pos = talker ? rope_pos : nullptr;
+            a.rope_axis = ctx->rope_axis;
             a.part = ctx->part;
             a.part_ml = ctx->part_ml;
             a.tickets = nullptr;  // the partials are merged by k_attn_merge (or a merge phase)
@@ -335,11 +339,11 @@ bool stage_params(dec_ctx* ctx, int l, int stage, int m, const float* x_in, Gemv
 // Launch stage `stage` of layer `l` for rows 0..m-1: one GEMV kernel, or for stage 1 the
 // attention chunks and the merge of their partials.
 cudaError_t launch_stage(dec_ctx* ctx, int l, int stage, int m, const float* x_in, cudaStream_t s,
-                         bool pdl) {
+                         bool pdl, const int32_t* rope_pos = nullptr) {
     if (stage < 0 || stage > 4) return cudaErrorInvalidValue;
     GemvParams g;
     AttnParams a;
-    if (!stage_params(ctx, l, stage, m, x_in, g, a))
+    if (!stage_params(ctx, l, stage, m, x_in, g, a, rope_pos))
         return launch_gemv(g, ctx->cfg.weight_dtype, ctx->num_sms, s, pdl);
     cudaError_t e = launch_attention(a, s, pdl);
     if (e != cudaSuccess) return e;
@@ -410,12 +414,14 @@ std::vector<StepPhase> build_phases(dec_ctx* ctx, int m) {
 // Enqueue the multi-kernel plan of one step on `s`: six kernels per layer, then the final
 // kernel.  Every kernel but the step's first is launched as a programmatic dependent of its
 // predecessor.
-cudaError_t enqueue_kernels(dec_ctx* ctx, int m, const float* x_in, float* out, cudaStream_t s) {
+cudaError_t enqueue_kernels(dec_ctx* ctx, int m, const float* x_in, float* out, cudaStream_t s,
+                            const int32_t* rope_pos) {
     const dec_config& c = ctx->cfg;
     cudaError_t e;
     for (int l = 0; l < c.layers; ++l)
         for (int stage = 0; stage < 5; ++stage)
-            if ((e = launch_stage(ctx, l, stage, m, x_in, s, l > 0 || stage > 0)) != cudaSuccess)
+            if ((e = launch_stage(ctx, l, stage, m, x_in, s, l > 0 || stage > 0, rope_pos)) !=
+                cudaSuccess)
                 return e;
     return launch_final(final_params(ctx, m, out), s, true);
 }
@@ -437,7 +443,7 @@ StepParams step_params(dec_ctx* ctx, const StepPhase* phases, const float* x_in,
 // K/V rows before its attention, which then runs in ATTN_PREFILL mode (row r sees keys up to
 // len + r).  The final kernel advances the stream by m.
 cudaError_t enqueue_prefill_block(dec_ctx* ctx, int stream, int m, const float* x_in, float* out,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, const int32_t* rope_pos) {
     const dec_config& c = ctx->cfg;
     cudaError_t e;
     for (int l = 0; l < c.layers; ++l)
@@ -445,7 +451,7 @@ cudaError_t enqueue_prefill_block(dec_ctx* ctx, int stream, int m, const float* 
             const bool pdl = l > 0 || stage > 0;
             GemvParams g;
             AttnParams a;
-            if (!stage_params(ctx, l, stage, m, x_in, g, a)) {
+            if (!stage_params(ctx, l, stage, m, x_in, g, a, rope_pos)) {
                 g.tap = nullptr;  // taps hold the last step's rows, not a block's
                 if ((e = launch_gemv(g, c.weight_dtype, ctx->num_sms, s, pdl)) != cudaSuccess) return e;
                 continue;
@@ -467,7 +473,7 @@ cudaError_t enqueue_prefill_block(dec_ctx* ctx, int stream, int m, const float* 
 // kernels one by one.
 cudaError_t enqueue_step(dec_ctx* ctx, const PlanEntry& pe, const float* x_in, float* out,
                          cudaStream_t s) {
-    if (!pe.phases) return enqueue_kernels(ctx, pe.m, x_in, out, s);
+    if (!pe.phases) return enqueue_kernels(ctx, pe.m, x_in, out, s, pe.rope);
     return launch_step(step_params(ctx, pe.phases, x_in, out), ctx->cfg.weight_dtype, pe.m,
                        ctx->cfg.head_dim, ctx->step_grid[pe.m], s);
 }
@@ -476,15 +482,20 @@ bool uses_persistent(const dec_ctx* ctx, int m) {
     return m >= 1 && m <= 2 && ctx->step_grid[m] > 0;
 }
 
-// The plan for (m, x_in, out): found in the cache or built (phase list uploaded, graph captured).
-PlanEntry* get_plan(dec_ctx* ctx, int m, const float* x_in, float* out, cudaError_t* err) {
+// The plan for (m, x_in, out, rope): found in the cache or built (phase list uploaded, graph
+// captured).  Steps with per-axis rotary positions take the multi-kernel plan.
+PlanEntry* get_plan(dec_ctx* ctx, int m, const float* x_in, float* out, const int32_t* rope,
+                    cudaError_t* err) {
     for (auto& e : ctx->plans)
-        if (e.m == m && (e.phases || (e.x_in == x_in && e.out == out))) return &e;
+        if (e.m == m && ((e.phases && !rope) ||
+                         (!e.phases && e.x_in == x_in && e.out == out && e.rope == rope)))
+            return &e;
     PlanEntry pe = {};
     pe.m = m;
     pe.x_in = x_in;
     pe.out = out;
-    if (uses_persistent(ctx, m)) {
+    pe.rope = rope;
+    if (!rope && uses_persistent(ctx, m)) {
         const std::vector<StepPhase> ph = build_phases(ctx, m);
         if (!ph.empty()) {
             const size_t bytes = ph.size() * sizeof(StepPhase);
@@ -553,9 +564,10 @@ dec_status check_step_args(dec_ctx* ctx, int m, const int32_t* pos) {
     return DEC_OK;
 }
 
-dec_status run_step(dec_ctx* ctx, int m, const float* x_in, float* out) {
+dec_status run_step(dec_ctx* ctx, int m, const float* x_in, float* out,
+                    const int32_t* rope = nullptr) {
     cudaError_t e = cudaSuccess;
-    PlanEntry* pe = get_plan(ctx, m, x_in, out, &e);
+    PlanEntry* pe = get_plan(ctx, m, x_in, out, rope, &e);
     if (!pe) return cuda_fail(ctx, e, "step plan");
     if (pe->exec && pe->phases && (pe->x_in != x_in || pe->out != out)) {
         // new input/output buffers: update the kernel node's arguments in place
@@ -768,6 +780,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     const size_t o_pr = talker ? 0 : take((size_t)c.layers * S * ctx->slots * 4);
     const size_t half = d / 2;
     const size_t o_cos = take((size_t)c.max_pos * half * 4), o_sin = take((size_t)c.max_pos * half * 4);
+    const size_t o_axis = take(half * 4);
     // a prefill block takes up to 8 rows, as many as the m > 2 GEMV's shared-memory stage allows
     if (talker) {
         const int widest = std::max(std::max(h, I), qw);
@@ -790,6 +803,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->pr = talker ? nullptr : reinterpret_cast<uint32_t*>(b + o_pr);
     ctx->rope_cos = reinterpret_cast<float*>(b + o_cos);
     ctx->rope_sin = reinterpret_cast<float*>(b + o_sin);
+    ctx->rope_axis = reinterpret_cast<int32_t*>(b + o_axis);  // zero: every frequency on axis t
     ctx->xres = reinterpret_cast<float*>(b + o_x);
     ctx->qkv = reinterpret_cast<float*>(b + o_qkv);
     ctx->attn = reinterpret_cast<float*>(b + o_att);
@@ -888,6 +902,11 @@ dec_status dec_prefill_kv(dec_ctx* ctx, int stream, const float* k, const float*
 }
 
 dec_status dec_prefill(dec_ctx* ctx, int stream, int n, const float* x, float* out) {
+    return dec_prefill_mrope(ctx, stream, n, x, nullptr, out);
+}
+
+dec_status dec_prefill_mrope(dec_ctx* ctx, int stream, int n, const float* x,
+                             const int32_t* rope_pos, float* out) {
     if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");
     if (ctx->cfg.kind != DEC_QWEN3_TALKER || ctx->prefill_rows < 1)
         return fail(ctx, DEC_E_UNSUPPORTED, "prefill blocks are a talker operation (a KV ring takes one position per step)");
@@ -895,6 +914,8 @@ dec_status dec_prefill(dec_ctx* ctx, int stream, int n, const float* x, float* o
         return fail(ctx, DEC_E_ARG, "stream %d outside 0..%d", stream, ctx->S - 1);
     if (n < 1 || !x || !out) return fail(ctx, DEC_E_ARG, "n < 1 or a NULL buffer");
     if (!aligned16(x) || !aligned16(out)) return fail(ctx, DEC_E_ARG, "x and out must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(rope_pos) & 3u)
+        return fail(ctx, DEC_E_ARG, "rope_pos must be 4-byte aligned");
     if ((long long)ctx->len_host[stream] + n > ctx->cfg.max_pos)
         return fail(ctx, DEC_E_CAPACITY, "stream %d: length %d + %d exceeds max_pos %d", stream,
                     ctx->len_host[stream], n, ctx->cfg.max_pos);
@@ -902,7 +923,7 @@ dec_status dec_prefill(dec_ctx* ctx, int stream, int n, const float* x, float* o
     for (int r0 = 0; r0 < n; r0 += ctx->prefill_rows) {
         const int m = std::min(ctx->prefill_rows, n - r0);
         CUDA_TRY(ctx, enqueue_prefill_block(ctx, stream, m, x + (size_t)r0 * h, out + (size_t)r0 * h,
-                                            ctx->stream),
+                                            ctx->stream, rope_pos ? rope_pos + 3 * (size_t)r0 : nullptr),
                  "prefill launch");
     }
     ctx->len_host[stream] += n;
@@ -922,7 +943,37 @@ dec_status dec_read_eos(dec_ctx* ctx, int m, float* dst_host) {
 }
 
 dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, float* hidden_out) {
+    return dec_step_mrope(ctx, m, x_in, pos, nullptr, hidden_out);
+}
+
+dec_status dec_set_mrope(dec_ctx* ctx, const int32_t* axis_host, int n) {
     if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");
+    if (ctx->cfg.kind != DEC_QWEN3_TALKER)
+        return fail(ctx, DEC_E_UNSUPPORTED, "multimodal rope is a talker operation");
+    const int half = ctx->cfg.head_dim / 2;
+    std::vector<int32_t> axis(half, 0);
+    if (axis_host) {
+        if (n != half) return fail(ctx, DEC_E_ARG, "the axis map has %d entries, head_dim/2 = %d", n, half);
+        for (int i = 0; i < half; ++i) {
+            if (axis_host[i] < 0 || axis_host[i] > 2)
+                return fail(ctx, DEC_E_ARG, "axis[%d] = %d outside 0..2", i, axis_host[i]);
+            axis[i] = axis_host[i];
+        }
+    }
+    CUDA_TRY(ctx, cudaMemcpyAsync(ctx->rope_axis, axis.data(), (size_t)half * 4,
+                                  cudaMemcpyHostToDevice, ctx->stream),
+             "axis map copy");
+    CUDA_TRY(ctx, cudaStreamSynchronize(ctx->stream), "axis map sync");
+    return DEC_OK;
+}
+
+dec_status dec_step_mrope(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos,
+                          const int32_t* rope_pos, float* hidden_out) {
+    if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");
+    if (rope_pos && ctx->cfg.kind != DEC_QWEN3_TALKER)
+        return fail(ctx, DEC_E_UNSUPPORTED, "multimodal rope is a talker operation");
+    if (reinterpret_cast<uintptr_t>(rope_pos) & 3u)
+        return fail(ctx, DEC_E_ARG, "rope_pos must be 4-byte aligned");
     dec_status st = check_step_args(ctx, m, pos);
     if (st != DEC_OK) return st;
     if (!x_in || !hidden_out) return fail(ctx, DEC_E_ARG, "x_in or hidden_out is NULL");
@@ -931,7 +982,7 @@ dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, 
     const char* a = reinterpret_cast<const char*>(x_in);
     const char* o = reinterpret_cast<const char*>(hidden_out);
     if (a < o + bytes && o < a + bytes) return fail(ctx, DEC_E_ARG, "x_in and hidden_out overlap");
-    return run_step(ctx, m, x_in, hidden_out);
+    return run_step(ctx, m, x_in, hidden_out, rope_pos);
 }
 
 dec_status dec_step_host(dec_ctx* ctx, int m, const float* x_in_host, const int32_t* pos,

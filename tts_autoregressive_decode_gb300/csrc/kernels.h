@@ -102,6 +102,11 @@ struct AttnParams {
     const float* rope_cos; // [max_pos][d/2]
     const float* rope_sin;
     int max_pos;
+    // TALKER/PREFILL, optional multimodal rope: the rows' rotary positions [rows][3] (t, h, w),
+    // each in 0..max_pos-1; rope frequency f turns by the position of axis rope_axis[f] (0..2).
+    // Null: every frequency turns by the row's cache position.
+    const int32_t* rope_pos;
+    const int32_t* rope_axis;  // [d/2]
     float* part;           // [m][H][max_chunks][d] partial outputs
     float* part_ml;        // [m][H][max_chunks][2] partial (max, sum)
     unsigned* tickets;     // [m][G] merge tickets, zero between calls; null: no in-kernel merge

@@ -34,6 +34,29 @@ def _ptr(t: torch.Tensor) -> int:
     return t.data_ptr()
 
 
+def _check_rope_pos(t: torch.Tensor, rows: int) -> None:
+    if t.dtype != torch.int32 or tuple(t.shape) != (rows, 3):
+        raise ValueError(f"rope_pos must be int32 [{rows}][3]")
+
+
+def mrope_axes(head_dim: int, sections: Sequence[int], interleaved: bool = True) -> List[int]:
+    """An axis map for Decoder.set_mrope from a (t, h, w) section split of the head_dim/2 rope
+    frequencies: interleaved puts h on frequencies 1, 4, 7, ... and w on 2, 5, 8, ... (each up
+    to its section) and t on the rest; contiguous gives t, then h, then w, in blocks."""
+    half = head_dim // 2
+    if len(sections) != 3 or sum(sections) != half or min(sections) < 0:
+        raise ValueError("three non-negative sections summing to head_dim/2")
+    if not interleaved:
+        return [0] * sections[0] + [1] * sections[1] + [2] * sections[2]
+    axes = [0] * half
+    for axis in (1, 2):
+        for i in range(axis, min(half, 3 * sections[axis]), 3):
+            axes[i] = axis
+    if [axes.count(a) for a in range(3)] != list(sections):
+        raise ValueError("the h and w sections do not fit an interleaved layout")
+    return axes
+
+
 def to_device(a: np.ndarray, device) -> torch.Tensor:
     """numpy float32 / uint16 (bf16 bit patterns) array -> device tensor with the same bytes."""
     a = np.ascontiguousarray(a)
@@ -109,15 +132,29 @@ class Decoder:
         L.check(self.lib.dec_prefill_kv(self.h, stream, _ptr(k), _ptr(v), n), self.h)
         self.sync()  # keep the sources alive until the copy has run
 
-    def prefill(self, stream: int, x: torch.Tensor, out: Optional[torch.Tensor] = None
-                ) -> torch.Tensor:
+    def prefill(self, stream: int, x: torch.Tensor, out: Optional[torch.Tensor] = None,
+                rope_pos: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Append the n rows of x [n][hidden] (device f32) to `stream` at its next positions and
-        return every position's final-norm hidden [n][hidden] (asynchronous)."""
+        return every position's final-norm hidden [n][hidden] (asynchronous).  rope_pos: the
+        rows' t, h, w rotary positions, device int32 [n][3] (multimodal rope)."""
         n = int(x.shape[0])
         if out is None:
             out = torch.empty_like(x)
-        L.check(self.lib.dec_prefill(self.h, stream, n, _ptr(x), _ptr(out)), self.h)
+        if rope_pos is None:
+            L.check(self.lib.dec_prefill(self.h, stream, n, _ptr(x), _ptr(out)), self.h)
+        else:
+            _check_rope_pos(rope_pos, n)
+            L.check(self.lib.dec_prefill_mrope(self.h, stream, n, _ptr(x), _ptr(rope_pos),
+                                               _ptr(out)), self.h)
         return out
+
+    def set_mrope(self, axes: Optional[Sequence[int]]) -> None:
+        """The axis (0 t, 1 h, 2 w) of each of the head_dim/2 rope frequencies (None: all t)."""
+        if axes is None:
+            L.check(self.lib.dec_set_mrope(self.h, None, 0), self.h)
+            return
+        a = (C.c_int32 * len(axes))(*[int(v) for v in axes])
+        L.check(self.lib.dec_set_mrope(self.h, a, len(axes)), self.h)
 
     def read_eos(self, m: int) -> np.ndarray:
         """The EOS logits of the last step of streams 0..m-1 (bias included); blocking."""
@@ -129,13 +166,20 @@ class Decoder:
         """Rows per prefill block (0: prefill not served)."""
         return int(self.lib.dec_prefill_block_rows(self.h))
 
-    def step(self, x: torch.Tensor, pos: Sequence[int], out: Optional[torch.Tensor] = None
-             ) -> torch.Tensor:
+    def step(self, x: torch.Tensor, pos: Sequence[int], out: Optional[torch.Tensor] = None,
+             rope_pos: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """One step of streams 0..m-1 (asynchronous); rope_pos: the rows' t, h, w rotary
+        positions, device int32 [m][3] (multimodal rope)."""
         m = int(x.shape[0])
         if out is None:
             out = torch.empty_like(x)
         p = (C.c_int32 * m)(*[int(v) for v in pos])
-        L.check(self.lib.dec_step(self.h, m, _ptr(x), p, _ptr(out)), self.h)
+        if rope_pos is None:
+            L.check(self.lib.dec_step(self.h, m, _ptr(x), p, _ptr(out)), self.h)
+        else:
+            _check_rope_pos(rope_pos, m)
+            L.check(self.lib.dec_step_mrope(self.h, m, _ptr(x), p, _ptr(rope_pos), _ptr(out)),
+                    self.h)
         return out
 
     def step_host(self, x: np.ndarray, pos: Sequence[int], out: Optional[np.ndarray] = None
