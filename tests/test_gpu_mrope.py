@@ -69,7 +69,7 @@ def test_uniform_axis_positions_equal_the_1d_step_bitwise(D):
     a = D.Decoder.from_synthetic(syn)
     b = D.Decoder.from_synthetic(syn)
     a.set_mrope(_axes(D, w))
-    for t in range(6):
+    for t in range(w.steps):
         pos = a.lengths(w.streams)
         r3 = torch.tensor([[p, p, p] for p in pos], dtype=torch.int32, device="cuda")
         x = torch.from_numpy(syn.inputs[t]).cuda()
@@ -112,6 +112,7 @@ def test_prefill_with_axis_positions_matches_oracle(D, name, n):
 def test_persistent_flag_steps_with_positions_run_the_kernel_chain(D):
     w = W.SMALL_TALKER_BF16
     syn = W.generate(w)
+    syn.max_pos = max(syn.max_pos, max(syn.lengths) + 10)
     a = D.Decoder.from_synthetic(syn, flags=D.L.DEC_FLAG_PERSISTENT)
     b = D.Decoder.from_synthetic(syn)
     axes = _axes(D, w)
@@ -121,7 +122,7 @@ def test_persistent_flag_steps_with_positions_run_the_kernel_chain(D):
     for t in range(8):
         m = 1 + t % 2
         pos = a.lengths(m)
-        x = torch.from_numpy(np.ascontiguousarray(syn.inputs[t][:m])).cuda()
+        x = torch.from_numpy(np.ascontiguousarray(syn.inputs[t % w.steps][:m])).cuda()
         if t % 3 == 2:  # a plain step in between: the persistent plan
             ya, yb = a.step(x, pos), b.step(x, pos)
         else:
