@@ -179,9 +179,9 @@ int dec_prefill_block_rows(const dec_ctx* ctx);
  *               must not overlap x_in
  * Asynchronous: enqueued on the context's stream, returns without waiting; x_in must not
  * change and hidden_out must not be read until the stream reaches this point.  The first
- * step with a given (m, x_in, hidden_out) captures a CUDA graph (milliseconds); later steps
- * replay it (up to 8 graphs are kept; with DEC_FLAG_PERSISTENT and m <= 2 one graph per m
- * serves every x_in / hidden_out pair).  Lengths advance by one on success; nothing changes on
+ * step of a given m captures a CUDA graph (milliseconds); later steps replay it, with new
+ * x_in / hidden_out pointers written into the graph's nodes that take them (up to 8 graphs
+ * are kept).  Lengths advance by one on success; nothing changes on
  * an error. */
 dec_status dec_step(dec_ctx* ctx, int m, const float* x_in, const int32_t* pos, float* hidden_out);
 

@@ -11,9 +11,10 @@
 //           -> [lin2 GEMV + LayerScale residual]; copy-out (+ length advance)
 // The sequence is the talker's build_step_plan and Mimi's transformer_shaped with the
 // elementwise passes folded into the GEMV prologues/epilogues and the attention prologue.
-// It is captured once per (m, x_in, hidden_out) as a CUDA graph and replayed; the per-step
-// positions live on the device and the graph's last kernel advances them, so a step needs no
-// host-to-device traffic beyond the caller's own input.
+// It is captured once per step width m as a CUDA graph and replayed, with the step's input and
+// output pointers patched into the few nodes that take them; the per-step positions live on
+// the device and the graph's last kernel advances them, so a step needs no host-to-device
+// traffic beyond the caller's own input.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -44,19 +45,26 @@ struct LayerW {
     const float *ln1_w, *ln1_b, *ln2_w, *ln2_b, *ls1, *ls2;
 };
 
-// A step plan.  Persistent plans (phases != null) serve every input/output pair of their m: the
-// pointers are arguments of the graph's single kernel node, updated in place when they change.
-// Multi-kernel plans are per (m, input, output) triple.  exec is null with DEC_FLAG_NO_GRAPH.
+// A step plan, one per (m, rotary-position buffer): it serves every input/output pair.  The
+// step's input and output pointers are arguments of a few kernel nodes of the captured graph,
+// updated in place when they change: the persistent kernel's single node, or in the multi-kernel
+// plan the three launches that take them (layer 0's q/k/v GEMV reads x_in, its o-proj adds
+// x_in as the residual, the final kernel writes the output).  exec is null with
+// DEC_FLAG_NO_GRAPH (the kernels are launched with the step's pointers each time).
 struct PlanEntry {
     int m;
-    const float* x_in;
+    const float* x_in;       // the pointers the graph's nodes hold now
     float* out;
     const int32_t* rope;     // per-axis rotary positions of the rows (multi-kernel plans), or null
     StepPhase* phases;       // device, or null (multi-kernel plan)
     cudaGraphExec_t exec;
-    cudaGraph_t graph;       // persistent plan: the captured graph, owner of `node`
+    cudaGraph_t graph;       // the captured graph, owner of the node handles below
     cudaGraphNode_t node;    // persistent plan: the kernel node
     cudaKernelNodeParams kp; // its launch parameters (kernelParams points at a StepParams)
+    cudaGraphNode_t io_node[3];       // multi-kernel plan: q/k/v GEMV, o-proj, final kernel
+    cudaKernelNodeParams io_kp[3];    // their launch parameters
+    GemvParams io_g[2];               // the two GEMVs' captured arguments
+    FinalParams io_f;                 // the final kernel's captured arguments
 };
 
 constexpr size_t kAlign = 256;
@@ -411,19 +419,73 @@ std::vector<StepPhase> build_phases(dec_ctx* ctx, int m) {
     return ph;
 }
 
+// The graph node the last launch captured on `s` became (null when `s` is not capturing).
+cudaGraphNode_t last_captured(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t n = 0;
+    if (cudaStreamGetCaptureInfo(s, &st, nullptr, nullptr, &deps, nullptr, &n) != cudaSuccess ||
+        st != cudaStreamCaptureStatusActive || n != 1)
+        return nullptr;
+    return deps[0];
+}
+
 // Enqueue the multi-kernel plan of one step on `s`: six kernels per layer, then the final
 // kernel.  Every kernel but the step's first is launched as a programmatic dependent of its
-// predecessor.
+// predecessor.  With `io` (under stream capture) the nodes of the three launches that take the
+// step's pointers are recorded in it.
 cudaError_t enqueue_kernels(dec_ctx* ctx, int m, const float* x_in, float* out, cudaStream_t s,
-                            const int32_t* rope_pos) {
+                            const int32_t* rope_pos, PlanEntry* io = nullptr) {
     const dec_config& c = ctx->cfg;
     cudaError_t e;
     for (int l = 0; l < c.layers; ++l)
-        for (int stage = 0; stage < 5; ++stage)
+        for (int stage = 0; stage < 5; ++stage) {
             if ((e = launch_stage(ctx, l, stage, m, x_in, s, l > 0 || stage > 0, rope_pos)) !=
                 cudaSuccess)
                 return e;
-    return launch_final(final_params(ctx, m, out), s, true);
+            if (io && l == 0 && (stage == 0 || stage == 2)) io->io_node[stage / 2] = last_captured(s);
+        }
+    if ((e = launch_final(final_params(ctx, m, out), s, true)) != cudaSuccess) return e;
+    if (io) io->io_node[2] = last_captured(s);
+    return cudaSuccess;
+}
+
+// After the capture of a multi-kernel plan: the recorded nodes' launch parameters and captured
+// arguments, checked against the pointers they must hold.
+cudaError_t record_io_nodes(PlanEntry& pe) {
+    for (int i = 0; i < 3; ++i) {
+        if (!pe.io_node[i]) return cudaErrorInvalidValue;
+        cudaError_t e = cudaGraphKernelNodeGetParams(pe.io_node[i], &pe.io_kp[i]);
+        if (e != cudaSuccess) return e;
+        if (!pe.io_kp[i].kernelParams || !pe.io_kp[i].kernelParams[0]) return cudaErrorInvalidValue;
+    }
+    memcpy(&pe.io_g[0], pe.io_kp[0].kernelParams[0], sizeof(GemvParams));
+    memcpy(&pe.io_g[1], pe.io_kp[1].kernelParams[0], sizeof(GemvParams));
+    memcpy(&pe.io_f, pe.io_kp[2].kernelParams[0], sizeof(FinalParams));
+    if (pe.io_g[0].x != pe.x_in || pe.io_g[1].res != pe.x_in || pe.io_f.out != pe.out)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+// Point a multi-kernel plan's graph at new input/output buffers.
+cudaError_t update_io_nodes(PlanEntry& pe, const float* x_in, float* out) {
+    GemvParams g0 = pe.io_g[0], g1 = pe.io_g[1];
+    FinalParams f = pe.io_f;
+    g0.x = x_in;
+    g1.res = x_in;
+    f.out = out;
+    void* a0[] = {&g0};
+    void* a1[] = {&g1};
+    void* a2[] = {&f};
+    void** args[3] = {a0, a1, a2};
+    for (int i = 0; i < 3; ++i) {
+        cudaKernelNodeParams kp = pe.io_kp[i];
+        kp.kernelParams = args[i];
+        kp.extra = nullptr;
+        cudaError_t e = cudaGraphExecKernelNodeSetParams(pe.exec, pe.io_node[i], &kp);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 StepParams step_params(dec_ctx* ctx, const StepPhase* phases, const float* x_in, float* out) {
@@ -471,9 +533,9 @@ cudaError_t enqueue_prefill_block(dec_ctx* ctx, int stream, int m, const float* 
 
 // Enqueue one step of a plan: the persistent kernel when the plan has a phase list, else the
 // kernels one by one.
-cudaError_t enqueue_step(dec_ctx* ctx, const PlanEntry& pe, const float* x_in, float* out,
-                         cudaStream_t s) {
-    if (!pe.phases) return enqueue_kernels(ctx, pe.m, x_in, out, s, pe.rope);
+cudaError_t enqueue_step(dec_ctx* ctx, PlanEntry& pe, const float* x_in, float* out,
+                         cudaStream_t s, bool record = false) {
+    if (!pe.phases) return enqueue_kernels(ctx, pe.m, x_in, out, s, pe.rope, record ? &pe : nullptr);
     return launch_step(step_params(ctx, pe.phases, x_in, out), ctx->cfg.weight_dtype, pe.m,
                        ctx->cfg.head_dim, ctx->step_grid[pe.m], s);
 }
@@ -487,9 +549,7 @@ bool uses_persistent(const dec_ctx* ctx, int m) {
 PlanEntry* get_plan(dec_ctx* ctx, int m, const float* x_in, float* out, const int32_t* rope,
                     cudaError_t* err) {
     for (auto& e : ctx->plans)
-        if (e.m == m && ((e.phases && !rope) ||
-                         (!e.phases && e.x_in == x_in && e.out == out && e.rope == rope)))
-            return &e;
+        if (e.m == m && e.rope == rope) return &e;
     PlanEntry pe = {};
     pe.m = m;
     pe.x_in = x_in;
@@ -512,7 +572,7 @@ PlanEntry* get_plan(dec_ctx* ctx, int m, const float* x_in, float* out, const in
             destroy_plan(pe);
             return nullptr;
         }
-        cudaError_t e = enqueue_step(ctx, pe, x_in, out, ctx->cap_stream);
+        cudaError_t e = enqueue_step(ctx, pe, x_in, out, ctx->cap_stream, true);
         cudaGraph_t graph = nullptr;
         cudaError_t e2 = cudaStreamEndCapture(ctx->cap_stream, &graph);
         if (e != cudaSuccess || e2 != cudaSuccess) {
@@ -526,12 +586,11 @@ PlanEntry* get_plan(dec_ctx* ctx, int m, const float* x_in, float* out, const in
             *err = cudaGraphGetNodes(graph, &pe.node, &n);
             if (*err == cudaSuccess && n != 1) *err = cudaErrorInvalidValue;
             if (*err == cudaSuccess) *err = cudaGraphKernelNodeGetParams(pe.node, &pe.kp);
+        } else {
+            *err = record_io_nodes(pe);
         }
         if (*err == cudaSuccess) *err = cudaGraphInstantiate(&pe.exec, graph, 0);
-        if (pe.phases)
-            pe.graph = graph;  // keeps the node handle valid for updates
-        else
-            cudaGraphDestroy(graph);
+        pe.graph = graph;  // keeps the node handles valid for updates
         if (*err != cudaSuccess) {
             destroy_plan(pe);
             return nullptr;
@@ -569,15 +628,23 @@ dec_status run_step(dec_ctx* ctx, int m, const float* x_in, float* out,
     cudaError_t e = cudaSuccess;
     PlanEntry* pe = get_plan(ctx, m, x_in, out, rope, &e);
     if (!pe) return cuda_fail(ctx, e, "step plan");
-    if (pe->exec && pe->phases && (pe->x_in != x_in || pe->out != out)) {
-        // new input/output buffers: update the kernel node's arguments in place
-        StepParams sp = step_params(ctx, pe->phases, x_in, out);
-        void* args[] = {&sp};
-        cudaKernelNodeParams kp = pe->kp;
-        kp.kernelParams = args;
-        kp.extra = nullptr;
-        e = cudaGraphExecKernelNodeSetParams(pe->exec, pe->node, &kp);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "step graph update");
+    if (pe->exec && (pe->x_in != x_in || pe->out != out)) {
+        // new input/output buffers: update the kernel nodes' arguments in place
+        if (pe->phases) {
+            StepParams sp = step_params(ctx, pe->phases, x_in, out);
+            void* args[] = {&sp};
+            cudaKernelNodeParams kp = pe->kp;
+            kp.kernelParams = args;
+            kp.extra = nullptr;
+            e = cudaGraphExecKernelNodeSetParams(pe->exec, pe->node, &kp);
+        } else {
+            e = update_io_nodes(*pe, x_in, out);
+        }
+        if (e != cudaSuccess) {  // the graph may hold a mix of old and new pointers: drop it
+            destroy_plan(*pe);
+            ctx->plans.erase(ctx->plans.begin() + (pe - ctx->plans.data()));
+            return cuda_fail(ctx, e, "step graph update");
+        }
         pe->x_in = x_in;
         pe->out = out;
     }
