@@ -240,11 +240,12 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv(const GemvParams p) {
 }
 
 // =============================================================================================
-// Split-K row-streaming GEMV for m <= 2 (the decode step's common case), on its own: the first
-// two weight batches are issued before griddepcontrol.wait (see gemv_rows.cuh).
+// Split-K row-streaming GEMV for m <= 8 (the decode step's common case), on its own: the first
+// two weight batches are issued before griddepcontrol.wait (see gemv_rows.cuh).  Two CTAs per
+// SM for m <= 2; one for wider rows, whose x slice and partial sums fill the register file.
 // =============================================================================================
 template <int DT, int MT, int NJ>
-__global__ void __launch_bounds__(kRowsThreads, 2) k_gemv_rows(const GemvParams p) {
+__global__ void __launch_bounds__(kRowsThreads, MT <= 2 ? 2 : 1) k_gemv_rows(const GemvParams p) {
     __shared__ float sh[rows_smem_floats<MT>()];
     using R = RowsGemv<DT, MT, NJ, 8>;
     uint4 wa[8], wb[8];
@@ -305,7 +306,7 @@ template <int DT, int MT, int NJ>
 static cudaError_t launch_rows_t(GemvParams p, int num_sms, cudaStream_t s, bool pdl) {
     p.unit = p.epi == EPI_SWIGLU ? 2 : 1;
     const int units = p.N / p.unit;
-    int grid = (p.per_sm > 0 ? p.per_sm : 2) * num_sms;
+    int grid = (p.per_sm > 0 ? p.per_sm : (MT <= 2 ? 2 : 1)) * num_sms;
     // at most kRowsMaxRows rows per CTA
     const int need = (p.N + kRowsMaxRows - 2) / (kRowsMaxRows - 1);
     if (grid < need) grid = need;
@@ -337,6 +338,12 @@ cudaError_t launch_gemv(const GemvParams& p, int dtype, int num_sms, cudaStream_
     const int nj = rows_gemv_nj(p.K, p.m, dtype);
     // bias, SiLU and the modulate prologue are served by the split-K kernel only
     if (!nj && (p.bias || p.act || p.pro == PRO_LN_MOD)) return cudaErrorInvalidValue;
+    if (nj && p.m > 2) {  // 3..8 rows, one granule a lane
+        if (dtype == 1) return p.m <= 4 ? launch_rows_t<1, 4, 1>(p, num_sms, s, pdl)
+                                        : launch_rows_t<1, 8, 1>(p, num_sms, s, pdl);
+        return p.m <= 4 ? launch_rows_t<0, 4, 1>(p, num_sms, s, pdl)
+                        : launch_rows_t<0, 8, 1>(p, num_sms, s, pdl);
+    }
     if (nj) {
         if (dtype == 1) return p.m <= 1 ? launch_rows_nj<1, 1>(p, nj, num_sms, s, pdl)
                                         : launch_rows_nj<1, 2>(p, nj, num_sms, s, pdl);

@@ -1,5 +1,5 @@
-// gemv_rows.cuh -- the split-K row-streaming GEMV for m <= 2 as device functions, shared by the
-// stand-alone kernel (gemv.cu) and the persistent step kernel (step.cu).
+// gemv_rows.cuh -- the split-K row-streaming GEMV for m <= 8 rows as device functions, shared by
+// the stand-alone kernel (gemv.cu) and the persistent step kernel (step.cu, m <= 2).
 //
 // y[r][n] = sum_k W[n][k] xin[r][k]; W row-major [N][K] (Qwen3-TTS talker on wgpu, MATVEC_SRC:
 // each weight is read once for all rows), f32 or bf16 bit patterns widened exactly.
@@ -146,11 +146,14 @@ struct RowsGemv {
             ok[j] = gj[j] < G;
         }
 
-        // The residual epilogue's operands of this thread's output (row tid / m, stream tid % m;
-        // a segment has at most kRowsMaxRows * 2 <= kRowsThreads outputs), fetched together with
-        // x rather than after the rows are summed.
+        // The residual epilogue's operands of this thread's output (row tid / m, stream tid % m),
+        // fetched together with x rather than after the rows are summed.  With m <= 2 a segment
+        // has at most kRowsMaxRows * 2 <= kRowsThreads outputs, one per thread; wider rows read
+        // them in the epilogue's loop instead.
+        constexpr bool kEpiPrefetch = MT <= 2;
         float res_v = 0.f, ls_v = 0.f, bias_v = 0.f;
         auto fetch_epi = [&](int seg) {
+            if constexpr (!kEpiPrefetch) return;
             const int srows = nrows - seg < kRowsMaxRows ? nrows - seg : kRowsMaxRows;
             if (tid < srows * m) {
                 const int row = row0 + seg + tid / m, mm = tid % m;
@@ -328,8 +331,8 @@ struct RowsGemv {
             // ---- cross-warp sums and the epilogue ------------------------------------------------
             const int rbase = row0 + seg;
             if (p.epi == EPI_SWIGLU) {
-                if (tid < (srows / 2) * m) {
-                    const int pr = tid / m, mm = tid - pr * m;
+                for (int o = tid; o < (srows / 2) * m; o += kRowsThreads) {
+                    const int pr = o / m, mm = o - pr * m;
                     float vg = 0.f, vu = 0.f;
                     for (int w = 0; w < kRowsWarps; ++w) {
                         vg += red[(w * kRowsMaxRows + 2 * pr) * MT + mm];
@@ -338,12 +341,19 @@ struct RowsGemv {
                     p.y[(size_t)mm * p.ldy + rbase / 2 + pr] = silu_f(vg) * vu;
                 }
             } else {
-                if (tid < srows * m) {
-                    const int r = tid / m, mm = tid - r * m;
+                for (int o = tid; o < srows * m; o += kRowsThreads) {
+                    const int r = o / m, mm = o - r * m;
                     float v = 0.f;
                     for (int w = 0; w < kRowsWarps; ++w) v += red[(w * kRowsMaxRows + r) * MT + mm];
-                    if (p.bias) v += bias_v;
                     const int row = rbase + r;
+                    if constexpr (!kEpiPrefetch) {
+                        if (p.bias) bias_v = p.bias[row];
+                        if (p.epi == EPI_RESID) {
+                            res_v = __ldcg(p.res + (size_t)mm * p.ldres + row);
+                            if (p.ls) ls_v = __ldcg(p.ls + row);
+                        }
+                    }
+                    if (p.bias) v += bias_v;
                     float out;
                     if (p.epi == EPI_RESID) {
                         const float tt = p.ls ? ls_v * v : v;
@@ -362,12 +372,15 @@ struct RowsGemv {
     }
 };
 
-// granules per lane of the split-K GEMV for this shape (0: not served by it)
+// granules per lane of the split-K GEMV for this shape (0: not served by it): up to 4 for
+// m <= 2; for 3..8 rows one granule (x of 8 rows then takes 64 registers a thread)
 inline int rows_gemv_nj(int K, int m, int dtype) {
     const int vec = dtype == 1 ? 8 : 4;
     const int per_pass = kRowsThreads * vec;  // elements one pass of the CTA covers
     const int nj = (K + per_pass - 1) / per_pass;
-    return (m <= 2 && nj >= 1 && nj <= 4) ? nj : 0;
+    if (nj < 1 || m < 1) return 0;
+    if (m <= 2) return nj <= 4 ? nj : 0;
+    return (m <= 8 && nj == 1) ? 1 : 0;
 }
 
 }  // namespace dec
