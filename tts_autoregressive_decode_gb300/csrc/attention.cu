@@ -83,8 +83,50 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(const AttnParams p) 
     if (tid == 0) p.tickets[r * p.G + g] = 0u;
 }
 
+// Two chunks per CTA: half h (128 threads, named barrier 1 + h) takes chunk 2 x + h of (kv
+// head y, row z); both halves stage their K/V rows before griddepcontrol.wait.  Each chunk is
+// computed as k_attention computes it; the partials are merged by k_attn_merge.
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads) k_attention_pair(const AttnParams p) {
+    extern __shared__ __align__(128) float smem[];
+    __shared__ __align__(8) uint64_t bar[2];
+    const int tid = threadIdx.x, h = tid >> 7, htid = tid & 127;
+    const int c = 2 * blockIdx.x + h, g = blockIdx.y, r = blockIdx.z;
+    const ChunkSmem sm = chunk_smem<D>(smem + (size_t)h * chunk_smem_floats(D));
+    const ChunkInfo ci = chunk_info(p, r, c);
+    const bool active = !ci.bad && c < ci.nch && c < p.max_chunks;
+    const uint32_t bar_h = smem_u32(&bar[h]);
+    if (htid == 0) {
+        mbar_init(bar_h, 1);
+        if (active) chunk_issue<D>(p, r, g, ci, sm, bar_h);
+    }
+    if (ci.bad && c == 0 && g == 0 && htid == 0) flag_check(p.status, CHECK_BOUNDS);
+    __syncthreads();  // both barriers initialised before any thread waits
+    pdl_trigger();
+    pdl_wait();
+    if (active) chunk_compute<D, kAttnThreads / 2>(p, r, g, c, ci, sm, bar_h, 0, htid, 1 + h);
+}
+
+// CTAs of k_attention_pair's grid: two chunks of the capacity per CTA, per kv head and row
+int attention_pair_ctas(const AttnParams& p) {
+    return ((p.max_chunks + 1) / 2) * p.G * p.m;
+}
+
 template <int D>
 static cudaError_t launch_t(const AttnParams& p, cudaStream_t s, bool pdl) {
+    if (p.paired && !p.tickets) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((p.max_chunks + 1) / 2, p.G, p.m);
+        cfg.blockDim = dim3(kAttnThreads);
+        cfg.dynamicSmemBytes = 2 * chunk_smem_bytes(D);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, k_attention_pair<D>, p);
+    }
     const size_t smem = attention_smem_bytes(D, p.H / p.G);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.max_chunks, p.G, p.m);
@@ -183,6 +225,11 @@ cudaError_t attention_configure() {
     cudaError_t e = cudaFuncSetAttribute(k_attention<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)attention_smem_bytes(64, kMaxGroup));
     if (e != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(k_attention_pair<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)(2 * chunk_smem_bytes(64)))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(k_attention_pair<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)(2 * chunk_smem_bytes(128)))) != cudaSuccess)
+        return e;
     return cudaFuncSetAttribute(k_attention<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)attention_smem_bytes(128, kMaxGroup));
 }

@@ -107,6 +107,9 @@ struct AttnParams {
     // Null: every frequency turns by the row's cache position.
     const int32_t* rope_pos;
     const int32_t* rope_axis;  // [d/2]
+    // 1: two chunks per CTA (k_attention_pair), for grids that then fit one wave at one CTA per
+    // SM; the chunks are computed exactly as by k_attention.  Not with tickets.
+    int paired;
     float* part;           // [m][H][max_chunks][d] partial outputs
     float* part_ml;        // [m][H][max_chunks][2] partial (max, sum)
     unsigned* tickets;     // [m][G] merge tickets, zero between calls; null: no in-kernel merge
@@ -116,6 +119,8 @@ struct AttnParams {
 };
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl);
+// CTAs of k_attention_pair's grid for these parameters
+int attention_pair_ctas(const AttnParams& p);
 cudaError_t attention_configure();
 // Merge of k_attention's chunk partials (launch after k_attention with tickets == nullptr).
 cudaError_t launch_attention_merge(const AttnParams& p, cudaStream_t s, bool pdl);
