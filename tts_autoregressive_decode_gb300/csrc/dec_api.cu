@@ -290,13 +290,13 @@ bool stage_params(dec_ctx* ctx, int l, int stage, int m, const float* x_in, Gemv
             a.max_pos = c.max_pos;
             a.rope_pos = talker ? rope_pos : nullptr;
             a.rope_axis = ctx->rope_axis;
-            // two chunks per CTA when that grid is one wave at one CTA per SM (a short cache,
-            // few streams); otherwise one chunk per CTA, up to three CTAs per SM
-            a.paired = attention_pair_ctas(a) <= ctx->num_sms ? 1 : 0;
             a.part = ctx->part;
             a.part_ml = ctx->part_ml;
             a.tickets = nullptr;  // the partials are merged by k_attn_merge (or a merge phase)
             a.max_chunks = ctx->max_chunks;
+            // two chunks per CTA when that grid is one wave at one CTA per SM (a short cache,
+            // few streams); otherwise one chunk per CTA, up to three CTAs per SM
+            a.paired = attention_pair_ctas(a) <= ctx->num_sms ? 1 : 0;
             a.out = ctx->attn;
             a.status = ctx->status;
             return true;
