@@ -168,6 +168,27 @@ def test_one_graph_serves_changing_buffers_bitwise(D, name):
     b.sync()
 
 
+@pytest.mark.parametrize("name", ["small_talker_f32", "small_talker_bf16"])
+def test_attention_grid_choice_leaves_results_unchanged(D, name):
+    """A small cache capacity gives the paired attention grid (two chunks per CTA, one wave);
+    a capacity of thousands of positions gives one chunk per CTA.  Every chunk is computed the
+    same way, so the two contexts agree bit for bit on the same steps."""
+    w = W.SMALL[name]
+    syn = W.generate(w)
+    big = W.generate(w)
+    big.max_pos = 64 * 2 * 160  # ceil(chunks / 2) * kv heads * streams > any SM count
+    a = D.Decoder.from_synthetic(syn)
+    b = D.Decoder.from_synthetic(big)
+    for t in range(w.steps):
+        x = torch.from_numpy(syn.inputs[t]).cuda()
+        pos = a.lengths()
+        ya, yb = a.step(x, pos), b.step(x, pos)
+        torch.cuda.synchronize()
+        assert torch.equal(ya, yb), (name, t)
+    a.sync()
+    b.sync()
+
+
 def test_kv_append_matches_oracle(D):
     w = W.SMALL_TALKER_F32
     syn = W.generate(w, steps=2)
