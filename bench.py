@@ -215,6 +215,23 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(pg, value: float, device) -> float:
+    """The largest of the ranks' values, e.g. the slowest rank's timed span (the value itself
+    with one rank).  `device` holds the reduction's tensor: "cuda" for NCCL, "cpu" for gloo."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, seconds: float) -> float:
+    """Whole-job steps per second: each of `world` replicas ran `steps` steps in at most
+    `seconds` (the max over ranks)."""
+    return world * steps / seconds
+
+
 def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
@@ -325,11 +342,7 @@ def run_ours(args):
         pg.barrier()
     clk = clocks.stop()
     dec.sync()
-    ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(pg, e0.elapsed_time(e1), "cuda")
     launches = args.steps * dec.kernels_per_step(m) + set_len_kernels[0]
 
     # bytes: mean over the steps actually timed (the talker's range cycles)
@@ -339,7 +352,7 @@ def run_ours(args):
     else:
         nb = step_bytes(w, [0] * m)
     ms_step = ms / args.steps
-    value = world * args.steps / (ms / 1e3)
+    value = job_throughput(world, args.steps, ms / 1e3)
     peak, peak_src = peaks()
     step_gbs = nb / (ms_step * 1e-3) / 1e9
 
@@ -462,12 +475,8 @@ def run_ours(args):
                     dec.truncate(s, base[s])
             p = (C.c_int32 * m)(*dec.lengths(m))
             dec.step_host_ptr(m, xh[t].data_ptr(), p, oh.data_ptr())
-        dt = time.perf_counter() - t0
-        if pg:
-            t = torch.tensor([dt], device="cuda")
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * args.steps / dt, "unit": "steps/s",
+        dt = max_over_ranks(pg, time.perf_counter() - t0, "cuda")
+        e2e = {"value": job_throughput(world, args.steps, dt), "unit": "steps/s",
                "h2d_bytes_per_step": m * h * 4, "d2h_bytes_per_step": m * h * 4 + 4}
 
     # ---- the oracle on the host cores (rank 0, one GPU only) -----------------------------------
