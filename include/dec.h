@@ -6,14 +6,19 @@
  *
  *   DEC_QWEN3_TALKER   the Qwen3-style TTS talker layer (Qwen3-TTS talker on wgpu,
  *                      inferencelayer qwen3tts_gpu.rs, build_step_plan): RMSNorm, q/k/v
- *                      row-major GEMVs, per-head q/k RMSNorm, 1-D rotate_half RoPE, KV
- *                      append, causal GQA attention over the whole cache, o-proj + residual,
- *                      RMSNorm, gate/up GEMVs + SwiGLU, down-proj + residual; final RMSNorm.
+ *                      row-major GEMVs, per-head q/k RMSNorm, 1-D rotate_half RoPE (or its
+ *                      multimodal form, dec_step_mrope), KV append, causal GQA attention over
+ *                      the whole cache, o-proj + residual, RMSNorm, gate/up GEMVs + SwiGLU,
+ *                      down-proj + residual; final RMSNorm.
  *   DEC_CODEC_WINDOWED the codec-style layer over a KV ring (Mimi on wgpu, inferencelayer
  *                      mimi_gpu.rs, transformer_shaped): LayerNorm, qkv GEMV, interleaved
  *                      RoPE + ring push + position stamp, windowed attention, out-proj with
  *                      LayerScale residual, LayerNorm, lin1 + GELU(erf), lin2 with LayerScale
- *                      residual; the output is the residual stream (no final norm).
+ *                      residual; the output is the residual stream (no final norm), or with
+ *                      the FlowLM head (Pocket TTS on wgpu) its final LayerNorm and EOS logit.
+ *
+ * Beside the step: batched causal prefill of talker blocks (dec_prefill), the flow head
+ * (dec_flow_*), and stateless GEMV / attention entry points.
  *
  * Every step of the path runs in this library's CUDA kernels.  Pointers are plain host or
  * device addresses as stated per argument; `void* stream` is a cudaStream_t (0 = legacy
