@@ -52,6 +52,7 @@ def lib(precision: str = "f32") -> C.CDLL:
         L.orc_matvec_f32.argtypes = [_fp, C.c_int, C.c_int, _dp, _dp]
         L.orc_matvec_bf16.argtypes = [C.POINTER(C.c_uint16), C.c_int, C.c_int, _dp, _dp]
         L.orc_rms_norm.argtypes = [_dp, _fp, C.c_int, C.c_double, _dp]
+        L.orc_matvec_bias.argtypes = [_fp, C.c_int, C.c_int, _dp, _fp, C.c_int, _dp]
         L.orc_layer_norm.argtypes = [_dp, _fp, _fp, C.c_int, C.c_double, _dp]
         L.orc_rope_table.argtypes = [C.c_int, C.c_double, C.c_int, _dp, _dp]
         L.orc_mrope_table.argtypes = [C.c_int, C.c_double, C.POINTER(C.c_int),
@@ -115,6 +116,19 @@ def matvec(W: np.ndarray, x, precision: str = "f32") -> np.ndarray:
         W = np.ascontiguousarray(W, dtype=np.float32)
         lib(precision).orc_matvec_f32(_ptr(W, C.c_float), N, K, _ptr(x, C.c_double),
                                       _ptr(y, C.c_double))
+    return y
+
+
+def matvec_bias(W: np.ndarray, x, b, act: int = 0, precision: str = "f32") -> np.ndarray:
+    """MV_BIAS (the flow head's linear): b[n] + sum_k W[n,k] x[k], accumulated from the bias in
+    ascending k, then SiLU when act == 1.  W float32 [N][K]."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    N, K = W.shape
+    x = _d(x)
+    y = np.empty(N, np.float64)
+    lib(precision).orc_matvec_bias(_ptr(W, C.c_float), N, K, _ptr(x, C.c_double),
+                                   _ptr(b, C.c_float), int(act), _ptr(y, C.c_double))
     return y
 
 

@@ -37,16 +37,18 @@ def build(force: bool = False, src: str = SRC, out_dir: str = HERE) -> None:
         out = os.path.join(out_dir, f"liboracle_{prec}.so")
         if not force and not _stale(out):
             continue
+        # a temporary name of this process: several test workers may build at once
+        tmp = f"{out}.{os.getpid()}.tmp"
         cmd = [
             "gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
             "-fno-fast-math", f"-DORC_REAL={real}", "-Wall", "-Wno-unknown-pragmas",
-            "-I", HERE, src, "-o", out + ".tmp", "-lm",
+            "-I", HERE, src, "-o", tmp, "-lm",
         ]
-        procs.append((subprocess.Popen(cmd), out))
-    for p, out in procs:
+        procs.append((subprocess.Popen(cmd), out, tmp))
+    for p, out, tmp in procs:
         if p.wait() != 0:
             raise RuntimeError(f"oracle build failed for {out}")
-        os.replace(out + ".tmp", out)
+        os.replace(tmp, out)  # atomic: a concurrent loader sees the old or the new library
 
 
 if __name__ == "__main__":

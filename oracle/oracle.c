@@ -90,6 +90,20 @@ static void matvec_r(const void* W, int bf16, int N, int K, const real* x, real*
     }
 }
 
+/* MV_BIAS (Pocket TTS on wgpu, the flow head): the accumulator starts at the bias,
+ * acc = b[n], then acc += W[n,k] x[k] for ascending k; with act == 1 the result goes through
+ * SiLU.  W is f32 row-major [N][K]. */
+static real silu_r(real g);
+static void matvec_bias_r(const float* W, int N, int K, const real* x, const float* b, int act,
+                          real* y) {
+    for (int n = 0; n < N; ++n) {
+        const float* row = W + (size_t)n * K;
+        real acc = (real)b[n];
+        for (int k = 0; k < K; ++k) acc += (real)row[k] * x[k];
+        y[n] = act == 1 ? silu_r(acc) : acc;
+    }
+}
+
 /* RMSNORM_SRC: inv = 1 / sqrt(sum(x^2) / n + eps); y = x * inv * w */
 static void rms_norm_r(const real* x, const float* w, int n, real eps, real* y) {
     real ss = 0;
@@ -263,6 +277,16 @@ void orc_matvec_bf16(const uint16_t* W, int N, int K, const double* x, double* y
     real* xr = to_real(x, K);
     real* yr = (real*)malloc(sizeof(real) * (size_t)N);
     matvec_r(W, 1, N, K, xr, yr);
+    from_real(yr, N, y);
+    free(xr);
+    free(yr);
+}
+
+void orc_matvec_bias(const float* W, int N, int K, const double* x, const float* b, int act,
+                     double* y) {
+    real* xr = to_real(x, K);
+    real* yr = (real*)malloc(sizeof(real) * (size_t)N);
+    matvec_bias_r(W, N, K, xr, b, act, yr);
     from_real(yr, N, y);
     free(xr);
     free(yr);
@@ -694,31 +718,30 @@ int orc_flow_step(const orc_flow* f, const float* cond, const float* noise, doub
         one[i] = 1.0f;
         zero[i] = 0.0f;
     }
-    /* x = input_proj(noise) */
+    /* x = input_proj(noise) (MV_BIAS) */
     for (int i = 0; i < Lt; ++i) t[i] = (real)noise[i];
-    matvec_r(f->ip_w, 0, D, Lt, t, x);
-    for (int i = 0; i < D; ++i) x[i] += (real)f->ip_b[i];
-    /* y = silu(t_const + cond_embed(cond)) */
+    matvec_bias_r(f->ip_w, D, Lt, t, f->ip_b, 0, x);
+    /* y = silu(t_const + cond_embed(cond)) (MV_BIAS, then ADD_SILU: the constant first) */
     for (int i = 0; i < C; ++i) t[i] = (real)cond[i];
-    matvec_r(f->cond_w, 0, D, C, t, y);
-    for (int i = 0; i < D; ++i) y[i] = silu_r((real)f->t_const[i] + (y[i] + (real)f->cond_b[i]));
+    matvec_bias_r(f->cond_w, D, C, t, f->cond_b, 0, y);
+    for (int i = 0; i < D; ++i) y[i] = silu_r((real)f->t_const[i] + y[i]);
     for (int bl = 0; bl < f->blocks; ++bl) {
-        matvec_r(f->ada_w[bl], 0, 3 * D, D, y, m);
-        for (int i = 0; i < 3 * D; ++i) m[i] += (real)f->ada_b[bl][i];
+        /* the fused adaLN projection [shift | scale | gate] */
+        matvec_bias_r(f->ada_w[bl], 3 * D, D, y, f->ada_b[bl], 0, m);
         layer_norm_r(x, f->ln_w[bl], f->ln_b[bl], D, eps, u);
         for (int i = 0; i < D; ++i) u[i] = u[i] * ((real)1 + m[D + i]) + m[i];  /* modulate */
-        matvec_r(f->m0_w[bl], 0, D, D, u, h);
-        for (int i = 0; i < D; ++i) h[i] = silu_r(h[i] + (real)f->m0_b[bl][i]);
-        matvec_r(f->m2_w[bl], 0, D, D, h, u);
-        for (int i = 0; i < D; ++i) x[i] += m[2 * D + i] * (u[i] + (real)f->m2_b[bl][i]);  /* gate */
+        matvec_bias_r(f->m0_w[bl], D, D, u, f->m0_b[bl], 1, h);
+        matvec_bias_r(f->m2_w[bl], D, D, h, f->m2_b[bl], 0, u);
+        for (int i = 0; i < D; ++i) x[i] += m[2 * D + i] * u[i];  /* GATED_ADD, third chunk */
     }
-    matvec_r(f->fada_w, 0, 2 * D, D, y, m);
-    for (int i = 0; i < 2 * D; ++i) m[i] += (real)f->fada_b[i];
+    /* final layer: [shift | scale] over a LayerNorm without affine weights */
+    matvec_bias_r(f->fada_w, 2 * D, D, y, f->fada_b, 0, m);
     layer_norm_r(x, one, zero, D, eps, u);
-    for (int i = 0; i < D; ++i) u[i] = u[i] * ((real)1 + m[D + i]) + m[i];
-    matvec_r(f->f_w, 0, Lt, D, u, dir);
-    for (int i = 0; i < Lt; ++i)  /* the LSD update with one step: x1 = x0 + dir / 1 */
-        out[i] = (double)((real)noise[i] + (dir[i] + (real)f->f_b[i]) / (real)1);
+    for (int i = 0; i < D; ++i) u[i] = u[i] * ((real)1 + m[D + i]) + m[i];  /* final modulate */
+    matvec_bias_r(f->f_w, Lt, D, u, f->f_b, 0, dir);
+    /* LSD_STEP with one step: x1 = x0 + dir * (1 / steps) */
+    const real inv_steps = (real)1 / (real)1;
+    for (int i = 0; i < Lt; ++i) out[i] = (double)((real)noise[i] + dir[i] * inv_steps);
     free(x); free(y); free(m); free(u); free(t); free(h); free(one); free(zero); free(dir);
     return 0;
 }

@@ -74,6 +74,10 @@ float orc_bf16_to_f32(uint16_t bits);
 void orc_matvec_f32(const float* W, int N, int K, const double* x, double* y);
 /* same with W given as bf16 bit patterns [N][K] */
 void orc_matvec_bf16(const uint16_t* W, int N, int K, const double* x, double* y);
+/* MV_BIAS: y[n] = b[n] + W[n,k] x[k] accumulated from the bias in ascending k; act == 1 applies
+ * SiLU to the result; W f32 [N][K] */
+void orc_matvec_bias(const float* W, int N, int K, const double* x, const float* b, int act,
+                     double* y);
 /* y = x / sqrt(mean(x^2) + eps) * w */
 void orc_rms_norm(const double* x, const float* w, int n, double eps, double* y);
 /* y = (x - mean) / sqrt(var + eps) * w + b, var biased */

@@ -47,6 +47,26 @@ MUTATIONS = [
      "rope_table_r(d, c->rope_theta, pos, cs, sn);\n"
      "    for (int gg = 0; gg < G; ++gg) rope_rotate_half_r(k + gg * d, d, cs, sn);"),
     ("mrope_rows_share_row0_positions", "pos3 ? pos3 + 3 * s : NULL", "pos3 ? pos3 : NULL"),
+    # the flow head (Pocket TTS on wgpu, PocketFlowGpu): adaLN chunk order and wiring
+    ("flow_shift_scale_swapped", "u[i] * ((real)1 + m[D + i]) + m[i];  /* modulate */",
+     "u[i] * ((real)1 + m[i]) + m[D + i];  /* modulate */"),
+    ("flow_modulate_one_dropped", "u[i] * ((real)1 + m[D + i]) + m[i];  /* modulate */",
+     "u[i] * m[D + i] + m[i];  /* modulate */"),
+    ("flow_gate_from_scale_chunk", "x[i] += m[2 * D + i] * u[i];", "x[i] += m[D + i] * u[i];"),
+    ("flow_final_norm_affine", "layer_norm_r(x, one, zero, D, eps, u);",
+     "layer_norm_r(x, f->ln_w[0], f->ln_b[0], D, eps, u);"),
+    ("flow_final_shift_scale_swapped",
+     "u[i] * ((real)1 + m[D + i]) + m[i];  /* final modulate */",
+     "u[i] * ((real)1 + m[i]) + m[D + i];  /* final modulate */"),
+    ("flow_bias_added_last", "real acc = (real)b[n];\n        for (int k = 0; k < K; ++k) acc += (real)row[k] * x[k];",
+     "real acc = 0;\n        for (int k = 0; k < K; ++k) acc += (real)row[k] * x[k];\n        acc += (real)b[n];"),
+    # the FlowLM head: the EOS logit reads the normalised row, not the residual stream
+    ("eos_reads_prenorm_row", "e += (real)m->eos_w[i] * y[i];", "e += (real)m->eos_w[i] * x[i];"),
+    # causal prefill: each row's key is appended before that row attends, and rows advance
+    ("row_attends_before_its_key_is_appended", "pos + 1, H, G,\n                    d, att, sc);",
+     "(pos > 0 ? pos : 1), H, G,\n                    d, att, sc);"),
+    ("prefill_rows_share_one_position", "        m->len[stream] += 1;\n    }\n    free(buf);",
+     "    }\n    m->len[stream] += n;\n    free(buf);"),
 ]
 
 PIN_FILES = ["test_oracle_pins.py", "test_oracle_mrope.py"]

@@ -428,24 +428,100 @@ def test_missing_layer_scale_is_a_scale_of_one():
         assert np.array_equal(a.step(syn.inputs[t], pos), b.step(syn.inputs[t], pos))
 
 
+def test_matvec_bias_starts_the_accumulator_at_the_bias():
+    """MV_BIAS (Pocket TTS on wgpu, the flow head): acc = b[n], then acc += w[n,k] x[k] in
+    ascending k, each step rounded to float32; act = 1 passes the sum through SiLU."""
+    r = _rng(31)
+    N, K = 7, 23
+    W = r.standard_normal((N, K)).astype(np.float32)
+    b = (100.0 * r.standard_normal(N)).astype(np.float32)   # large: the order shows in the bits
+    x = r.standard_normal(K).astype(np.float32)
+    want = np.empty(N, np.float32)
+    for n in range(N):
+        acc = np.float32(b[n])
+        for k in range(K):
+            acc = np.float32(acc + np.float32(W[n, k] * x[k]))
+        want[n] = acc
+    got = oracle.matvec_bias(W, x, b)
+    assert np.array_equal(got, want.astype(np.float64))
+    # the bias-last order rounds differently on at least one row of this case
+    last = (_f32(oracle.matvec(W, x)) + b).astype(np.float64)
+    assert not np.array_equal(got, last)
+    s = oracle.matvec_bias(W, x, b, act=1)
+    assert np.array_equal(s, np.array([oracle.silu(float(v)) for v in want], np.float64))
+
+
 def _flow_by_primitives(f, d, cond, noise):
     """The flow head's LSD step composed from individually pinned oracle primitives, one
     float32 rounding per operation, in the order of the page's dispatch plan."""
     f32 = np.float32
     sil = lambda v: _f32([oracle.silu(float(t)) for t in v])
-    x = _f32(oracle.matvec(d["ip_w"], noise)) + d["ip_b"]
-    y = sil(d["t_const"] + (_f32(oracle.matvec(d["cond_w"], cond)) + d["cond_b"]))
+    mvb = lambda w, x, b, act=0: _f32(oracle.matvec_bias(w, x, b, act))
+    x = mvb(d["ip_w"], noise, d["ip_b"])
+    y = sil(d["t_const"] + mvb(d["cond_w"], cond, d["cond_b"]))
     D = f.dim
     for i in range(f.blocks):
-        m = _f32(oracle.matvec(d[f"ada_w{i}"], y)) + d[f"ada_b{i}"]
+        m = mvb(d[f"ada_w{i}"], y, d[f"ada_b{i}"])
         u = _f32(oracle.layer_norm(x, d[f"ln_w{i}"], d[f"ln_b{i}"], f.ln_eps))
         u = u * (f32(1) + m[D:2 * D]) + m[:D]
-        h = sil(_f32(oracle.matvec(d[f"m0_w{i}"], u)) + d[f"m0_b{i}"])
-        x = x + m[2 * D:] * (_f32(oracle.matvec(d[f"m2_w{i}"], h)) + d[f"m2_b{i}"])
-    m = _f32(oracle.matvec(d["fada_w"], y)) + d["fada_b"]
+        h = mvb(d[f"m0_w{i}"], u, d[f"m0_b{i}"], 1)
+        x = x + m[2 * D:] * mvb(d[f"m2_w{i}"], h, d[f"m2_b{i}"])
+    m = mvb(d["fada_w"], y, d["fada_b"])
     u = _f32(oracle.layer_norm(x, np.ones(D, np.float32), np.zeros(D, np.float32), f.ln_eps))
     u = u * (f32(1) + m[D:]) + m[:D]
-    return noise + (_f32(oracle.matvec(d["f_w"], u)) + d["f_b"]) / f32(1)
+    return noise + mvb(d["f_w"], u, d["f_b"]) * f32(1)
+
+
+def test_flow_head_adaln_wiring_closed_form():
+    """The page fixes the fused adaLN projection as [shift | scale | gate], modulate as
+    x (1 + scale) + shift, the gate on the third chunk multiplying the block's MLP branch, and a
+    final [shift | scale] over a LayerNorm WITHOUT affine weights (Pocket TTS on wgpu,
+    PocketFlowGpu::new, MODULATE, GATED_ADD).  With zero projection matrices every chunk is its
+    bias, with identity MLP matrices the branch is silu(modulate(LN(x0))), and with a selection
+    matrix as the final linear the output is closed-form in float64: no value below comes from
+    the oracle.  Shift, scale and gate are distinct, so any swap or dropped term moves it."""
+    D, Lt, C_ = 12, 5, 9
+    r = _rng(41)
+    x0 = r.standard_normal(D).astype(np.float32)
+    shift = (0.3 * r.standard_normal(D)).astype(np.float32)
+    scale = (0.5 + 0.3 * r.standard_normal(D)).astype(np.float32)
+    gate = (-0.7 + 0.2 * r.standard_normal(D)).astype(np.float32)
+    fshift = (0.2 * r.standard_normal(D)).astype(np.float32)
+    fscale = (-0.4 + 0.2 * r.standard_normal(D)).astype(np.float32)
+    lnw = (1.0 + 0.3 * r.standard_normal(D)).astype(np.float32)
+    lnb = (0.2 * r.standard_normal(D)).astype(np.float32)
+    sel = np.zeros((Lt, D), np.float32)
+    sel[np.arange(Lt), 2 * np.arange(Lt)] = 1.0            # out j reads feature 2 j
+    z = lambda *s: np.zeros(s, np.float32)
+    d = {"ip_w": z(D, Lt), "ip_b": x0, "cond_w": z(D, C_), "cond_b": z(D),
+         "t_const": r.standard_normal(D).astype(np.float32),
+         "ada_w0": z(3 * D, D), "ada_b0": np.concatenate([shift, scale, gate]),
+         "ln_w0": lnw, "ln_b0": lnb,
+         "m0_w0": np.eye(D, dtype=np.float32), "m0_b0": z(D),
+         "m2_w0": np.eye(D, dtype=np.float32), "m2_b0": z(D),
+         "fada_w": z(2 * D, D), "fada_b": np.concatenate([fshift, fscale]),
+         "f_w": sel, "f_b": z(Lt)}
+    import dataclasses
+    f = dataclasses.replace(W.SMALL_FLOW, dim=D, latent=Lt, cond=C_, blocks=1)
+    noise = r.standard_normal(Lt).astype(np.float32)
+    cond = r.standard_normal(C_).astype(np.float32)
+    got = oracle.flow_step(f, d, cond, noise)
+
+    e = np.float64
+    eps = f.ln_eps
+
+    def ln(v):
+        v = v.astype(e)
+        mu = v.mean()
+        return (v - mu) / np.sqrt(((v - mu) ** 2).mean() + eps)
+
+    silu = lambda v: v / (1.0 + np.exp(-v))
+    u = ln(x0) * lnw.astype(e) + lnb.astype(e)                  # affine block LayerNorm
+    u = u * (1.0 + scale.astype(e)) + shift.astype(e)            # modulate
+    x1 = x0.astype(e) + gate.astype(e) * silu(u)                 # identity m0 (SiLU), m2, gate
+    v = ln(x1) * (1.0 + fscale.astype(e)) + fshift.astype(e)     # final: no affine weights
+    want = noise.astype(e) + v[2 * np.arange(Lt)]
+    assert np.max(np.abs(got - want)) <= 2e-6 * (1.0 + np.max(np.abs(want)))
 
 
 def test_flow_head_is_the_page_order_of_pinned_primitives():
