@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # reports null until it is captured again.
 NCU_TRAFFIC = {
     # gate/up GEMV (k_gemv_rows<bf16, m1, NJ1>, N = 12288, K = 2048): one launch captured with
-    # ncu --set full on the 2-layer case of the same shapes (profiles/k_gemv_rows_gateup_*.md);
-    # a launch does the same work at any layer count
+    # ncu --set full on the 2-layer case of the same shapes; a launch does the same work at any
+    # layer count
     W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_384_640, "source_sha": "71f033a846d5ab70"},
 }
 
@@ -66,6 +66,8 @@ def parse():
     p.add_argument("--plan", choices=["kernels", "persistent"], default="kernels",
                    help="step plan: the chain of kernels (default) or the persistent kernel")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--streams8", type=int, default=1,
+                   help="also time the 8-stream 28-layer workload (1, default) or not (0)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
@@ -232,6 +234,37 @@ def job_throughput(world: int, steps: int, seconds: float) -> float:
     return world * steps / seconds
 
 
+def bench_config(w: W.Workload, lengths, world: int) -> dict:
+    """The workload as both arms state it (the same dict, so the two lines compare)."""
+    talker = w.kind == "talker"
+    nb = step_bytes(w, lengths if talker else [0] * w.streams)
+    return {"workload": w.name, "layers": w.layers, "hidden": w.hidden,
+            "heads": f"{w.q_heads}/{w.kv_heads}", "head_dim": w.head_dim, "inter": w.inter,
+            "weights": w.weight_dtype, "kv": "f32", "streams": w.streams,
+            "positions": (f"{list(lengths)}..+{w.steps - 1}, replayed cyclically" if talker
+                          else f"from {list(lengths)}, continuing"),
+            "l2": ("no flush: per-step working set %.2f GB >> 129 MB L2" % (nb / 1e9)
+                   if nb > 4 * 129e6 else
+                   "per-step working set %.1f MB may be partly L2-resident" % (nb / 1e6)),
+            "parallelism": f"replicas x{world}"}
+
+
+def cpu_baselines(syn, seconds: float, one_core_seconds: float):
+    """The oracle timed twice on the host (SURVEY's plan): the sequential oracle on one core,
+    and the row-parallel build of the same oracle on every core (bitwise the same results)."""
+    w = syn.workload
+    threads = os.cpu_count() or 1
+    n, dt = oracle_rate(syn, seconds, threads)
+    all_cores = {"value": n / dt, "unit": "steps/s", "cores": threads,
+                 "sample": f"the first {n} steps of {w.name} (positions from the workload start), "
+                           f"{dt:.1f} s on {threads} threads"}
+    n1, dt1 = oracle_rate(syn, one_core_seconds, 1)
+    one_core = {"value": n1 / dt1, "unit": "steps/s", "cores": 1,
+                "sample": f"the first {n1} steps of {w.name}, {dt1:.1f} s on 1 thread"}
+    return {"value": all_cores["value"], "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "sample": all_cores["sample"], "all_cores": all_cores, "one_core": one_core}
+
+
 def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
@@ -249,6 +282,11 @@ def run_reference(args):
     n, dt = oracle_rate(syn, 1e9, threads, max_steps=args.steps, layers=layers)
     per_step = dt / n * (w.layers / layers)       # full-stack equivalent seconds per step
     value = 1.0 / per_step
+    # the sequential oracle on one core: one step of the same sample size
+    n1, dt1 = oracle_rate(syn, 0.0, 1, max_steps=1, layers=layers)
+    one_core = {"value": n1 / (dt1 * (w.layers / layers)), "unit": "steps/s", "cores": 1,
+                "sample": f"{n1} step" + (f" on the first {layers} layers, scaled" if layers < w.layers
+                                          else "") + ", 1 thread"}
     sample = (f"{n} steps of the {w.layers}-layer workload"
               + (f", each timed on its first {layers} layers and scaled by {w.layers}/{layers}"
                  if layers < w.layers else "")
@@ -258,12 +296,63 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "streams": w.streams},
+        "config": bench_config(w, syn.lengths, 1),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "one_core": one_core},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
+
+
+def time_streams8(args, stream, peak):
+    """The 8-stream workload (28-layer bf16 talker, lengths U[512, 4096], 64 steps): K steps of
+    its position range, replayed cyclically like the main workload, between CUDA events."""
+    import torch
+
+    from tts_autoregressive_decode_gb300.decoder import Decoder
+
+    w = W.TALKER_H2048_L28_M8
+    syn = W.generate(w)
+    dec = Decoder.from_synthetic(syn)
+    m, base = w.streams, list(syn.lengths)
+    X = torch.from_numpy(syn.inputs).cuda()
+    out = torch.empty((m, w.hidden), dtype=torch.float32, device="cuda")
+    del syn
+
+    def one(i):
+        t = i % w.steps
+        if t == 0 and dec.length(0) != base[0]:
+            for s_ in range(m):
+                dec.truncate(s_, base[s_])
+        dec.step(X[t], dec.lengths(m), out)
+
+    for i in range(max(3, args.warmup)):
+        one(i)
+    dec.sync()
+    for s_ in range(m):
+        dec.truncate(s_, base[s_])
+    dec.sync()
+    steps = max(1, min(args.steps, 4 * w.steps))
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dec.sync()
+    ms = e0.elapsed_time(e1) / steps
+    per = [step_bytes(w, [b + (i % w.steps) for b in base]) for i in range(w.steps)]
+    nb = sum(per[i % w.steps] for i in range(steps)) / steps
+    gbs = nb / (ms * 1e-3) / 1e9
+    kpl = dec.kernels_per_step(m)
+    dec.close()
+    return {"workload": w.name, "streams": m, "lengths": base, "steps": steps,
+            "ms_per_step": ms, "steps_per_s": 1e3 / ms, "tokens_per_s": m * 1e3 / ms,
+            "bytes_per_step": nb, "achieved_hbm_gbs": gbs, "frac_of_peak": gbs / peak,
+            "kernels_per_step": kpl,
+            "note": "weights read once per step for all 8 rows, plus each stream's K/V"}
 
 
 def run_ours(args):
@@ -457,6 +546,11 @@ def run_ours(args):
                 "note": "one LSD step conditioned in place on the step's output row"}
         head.close()
 
+    # ---- 8 concurrent streams of the 28-layer talker (its own decoder, timed the same way) ------
+    streams8 = None
+    if args.streams8 and w.name == W.TALKER_H2048_L28.name and not args.layers:
+        streams8 = time_streams8(args, stream, peak)
+
     # ---- end to end through the C ABI with host buffers ----------------------------------------
     e2e = None
     if not args.no_e2e:
@@ -482,30 +576,18 @@ def run_ours(args):
     # ---- the oracle on the host cores (rank 0, one GPU only) -----------------------------------
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        threads = os.cpu_count() or 1
-        n, dt = oracle_rate(syn, args.cpu_seconds, threads)
-        cpu = {"value": n / dt, "unit": "steps/s", "cores": threads, "kind": "oracle",
-               "sample": f"the first {n} steps of {w.name} (positions from the workload start), "
-                         f"{dt:.1f} s on {threads} threads"}
+        cpu = cpu_baselines(syn, args.cpu_seconds, args.cpu_seconds)
 
     if rank != 0:
         return
-    cfg = {"workload": w.name, "layers": w.layers, "hidden": w.hidden,
-           "heads": f"{w.q_heads}/{w.kv_heads}", "head_dim": w.head_dim, "inter": w.inter,
-           "weights": w.weight_dtype, "kv": "f32", "streams": m,
-           "positions": (f"{pos_before}..+{w.steps - 1}, replayed cyclically" if talker
-                         else f"from {pos_before}, continuing"),
-           "l2": ("no flush: per-step working set %.2f GB >> 129 MB L2" % (nb / 1e9)
-                  if nb > 4 * 129e6 else
-                  "per-step working set %.1f MB may be partly L2-resident" % (nb / 1e6)),
-           "graph": ("one CUDA graph per step holding one cooperative persistent kernel" if kpl == 1
-                     else "one CUDA graph per step, 6 PDL-chained kernels per layer + 1"),
-           "parallelism": f"replicas x{world}"}
+    cfg = bench_config(w, base, world)
+    plan = ("one CUDA graph per step holding one cooperative persistent kernel" if kpl == 1
+            else f"one CUDA graph per step, {kpl} PDL-chained kernels")
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": cfg,
+        "data": "synthetic", "config": cfg, "plan": plan,
         "tokens_per_s": value * m,
         "achieved_hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak,
         "bytes_per_step": nb,
@@ -522,6 +604,7 @@ def run_ours(args):
                           "frac": step_gbs / peak, "bytes_per_step": nb},
         "gpu_launches": launches,
         "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "prefill": prefill, "flow_head": flow,
+        "streams8": streams8,
     }
     print(json.dumps(line))
     if pg:

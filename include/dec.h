@@ -358,16 +358,24 @@ dec_status dec_attention(int m, int q_heads, int kv_heads, int head_dim, int cap
  * cudaMalloc/cudaFree may synchronize the device and take unbounded time, and code inside a host
  * application whose own allocator owns the device-memory budget.  This entry computes exactly
  * what dec_attention computes, with the same arguments minus the workspace: its scratch is a
- * static device array of 4 MiB that the library holds on every GPU it is loaded on until the
- * process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ * static device array of 4 MiB (4194304 bytes) that the library holds on every GPU it is
+ * loaded on until the process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
  *   Limit: the scratch dec_attention_workspace_bytes(m, q_heads, kv_heads, head_dim, capacity)
- *   would report must fit in 4 MiB (e.g. m = 1, 16 q heads, d = 128: capacity up to 32768);
- *   larger requests return DEC_E_UNSUPPORTED (text in dec_last_error(NULL)).
- *   The first call on a device looks up the array's device address; make that first call
- *   outside any stream capture.
+ *   reports must fit in the 4 MiB.  Example: m = 1, 16 q heads, 8 kv heads, d = 128 takes
+ *   capacity up to 32256 (504 chunks of 64 keys: 4128768 bytes of partial outputs, 64512 of
+ *   partial maxima and sums, 256 of merge tickets); capacity 32257 needs a 505th chunk and is
+ *   rejected.  Larger requests return DEC_E_UNSUPPORTED (text in dec_last_error(NULL)).
+ *   When the array is reserved: with the default lazy loading of CUDA modules, the library's
+ *   module, and with it the array, is loaded on a device at the first call of this entry (or of
+ *   any other entry point) on that device; that first call also looks up the array's device
+ *   address.  Make that first call outside any stream capture, and early if the reservation of
+ *   4 MiB must not happen on a time-critical path.
  *   Every call on a device shares the one array: calls that overlap on the GPU (other streams,
  *   other host threads) race and corrupt each other's results.  Each call clears the words that
  *   must start at zero before its kernel runs.
+ *   lens[r] outside 1..capacity is not reported by this entry (it has no status word the caller
+ *   could read): the rows of such a stream are left unwritten, so out[r] is undefined.
  * Asynchronous on `stream`; same layouts, limits and errors as dec_attention otherwise. */
 dec_status dec_attention_noalloc(int m, int q_heads, int kv_heads, int head_dim, int capacity,
                                  const float* q, const float* k, const float* v,

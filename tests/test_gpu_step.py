@@ -120,10 +120,25 @@ def test_talker_h2048_l28_bf16_128_steps(D):
     print(rep[-1])
 
 
-def test_talker_h2048_l28_bf16_m8_first_steps(D):
-    # 8 streams, lengths U[512, 4096]; the oracle runs the first 3 of the 64 steps
+@pytest.mark.slow
+def test_talker_h2048_l28_bf16_m8_every_step(D):
+    # 8 streams, lengths U[512, 4096]: every row of all 64 steps against the oracle
     rep = []
-    run_parity(D, W.TALKER_H2048_L28_M8, steps=3, report=rep)
+    run_parity(D, W.TALKER_H2048_L28_M8, report=rep)
+    print(rep[-1])
+
+
+def test_talker_h2048_l28_bf16_m8_last_steps(D):
+    # The same 8-stream stack brought to the last positions of its 64 steps directly: each
+    # stream is prefilled to its length + 61, then steps 61..63 run on both sides.  The longest
+    # stream passes 4096 positions here, and every stream crosses its own chunk boundaries.
+    import dataclasses
+    w = W.TALKER_H2048_L28_M8
+    late = dataclasses.replace(w, name=w.name + "_last3", prefill_range=None,
+                               prefill=tuple(n + 61 for n in W.prefill_lengths(w)), steps=3)
+    assert W.max_pos(late) == W.max_pos(w) and max(late.prefill) + 2 >= 4096
+    rep = []
+    run_parity(D, late, report=rep)
     print(rep[-1])
 
 

@@ -73,3 +73,25 @@ def test_oversized_request_is_rejected(lib):
                                           torch.cuda.current_stream().cuda_stream)
     assert st == lib.DEC_E_UNSUPPORTED
     assert b"static scratch" in lib.load().dec_last_error(None)
+
+
+def test_capacity_at_the_exact_limit(lib):
+    # m = 1, 16/8 heads, d = 128: 504 chunks of 64 keys fill the 4 MiB array (capacity 32256);
+    # one key more needs a 505th chunk and is rejected with the state of the array untouched
+    m, H, G, d = 1, 16, 8, 128
+    L = lib.load()
+    assert L.dec_attention_workspace_bytes(m, H, G, d, 32256) <= 4 << 20
+    assert L.dec_attention_workspace_bytes(m, H, G, d, 32257) > 4 << 20
+    q, k, v, Ld, cap = _case(4, m, H, G, d, [32256])
+    assert cap >= 32256
+    k, v = k[:, :, :32256].contiguous(), v[:, :, :32256].contiguous()
+    got = _noalloc(lib, m, H, G, d, 32256, q, k, v, Ld)
+    want = _with_workspace(lib, m, H, G, d, 32256, q, k, v, Ld)
+    torch.cuda.synchronize()
+    assert float((got - want).abs().max()) <= 2e-5
+    out = torch.empty_like(q)
+    st = L.dec_attention_noalloc(m, H, G, d, 32257, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                 Ld.data_ptr(), out.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert st == lib.DEC_E_UNSUPPORTED
+    assert b"static scratch" in L.dec_last_error(None)
