@@ -450,7 +450,8 @@ def run_ours(args):
     k_alone_ms = None
     if kpl == 1:
         # the persistent step kernel is the whole step: its launches are the timed region's
-        kname = "persistent step kernel (k_step: all layers' GEMVs, attention, merge, output)"
+        kname = ("persistent streamed step kernel (k_stream_step: every layer's GEMVs, "
+                 "attention, merge and the output rows)")
         kbytes = nb
         k_ms = ms_step
     else:

@@ -56,8 +56,10 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1 } dec_dtype;
 #define DEC_FLAG_TAPS 1u     /* keep the residual stream after every layer (dec_read_tap) */
 #define DEC_FLAG_NO_GRAPH 2u /* launch kernels one by one instead of replaying a CUDA graph */
 #define DEC_FLAG_PERSISTENT 4u /* steps of m <= 2 rows run as one persistent cooperative kernel
-                                  whose phases are separated by grid-wide barriers, instead of
-                                  the default chain of kernels; same results, bit for bit */
+                                  (the streamed step: every SM streams its share of the weights
+                                  and K/V through a shared-memory ring while its consumer warps
+                                  wait on tagged activations) instead of the chain of kernels;
+                                  results agree within floating-point rounding */
 
 /*
  * Model geometry.  Talker fields follow the talker's Dims (Qwen3-TTS talker on wgpu, `Dims`
@@ -252,6 +254,21 @@ dec_status dec_read_eos(dec_ctx* ctx, int m, float* dst_host);
 /* Number of CUDA kernels one step of m rows launches (for launch accounting): 6 * layers + 1,
  * or 1 when the persistent kernel serves the step (DEC_FLAG_PERSISTENT, m <= 2). */
 int dec_kernels_per_step(const dec_ctx* ctx, int m);
+
+/* Failure-path check of the persistent kernel's bounded waits (no counterpart on the pages).
+ * The NEXT step of m <= 2 rows that the persistent kernel serves runs once outside the CUDA graph
+ * with the consumers of phase `phase` (0 .. 5 * layers; per layer: q/k/v, attention with the
+ * merge of its partials, o-proj, gate/up, down; then the output rows) waiting for activation
+ * tags that no CTA writes,
+ * and with every wait of that step bounded by `polls` loads (>= 1; about a microsecond each;
+ * too small a bound also cuts the step's ordinary waits short).  The wait runs out, the
+ * kernel flags its check word and every CTA leaves early after its copies in flight have landed:
+ * nothing faults or hangs.  That step's output and its cache rows are undefined; the next
+ * dec_sync returns DEC_E_DEVICE_CHECK (wait limit) and clears the check word.  The stream length
+ * still advances, so a caller rewinds with dec_truncate (talker) before stepping on.  Phases
+ * that wait on no activation (layer 0's q/k/v reads the step input) do not run out.
+ * Errors: DEC_E_ARG (phase or polls out of range), DEC_E_UNSUPPORTED (no persistent plan). */
+dec_status dec_inject_stall(dec_ctx* ctx, int phase, int polls);
 
 /* Talker only: shorten stream `stream` to `new_len` positions (0 <= new_len <= its length), so
  * the next step is at position new_len.  Cache rows below new_len are kept (rows at and above

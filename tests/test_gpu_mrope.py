@@ -123,13 +123,16 @@ def test_persistent_flag_steps_with_positions_run_the_kernel_chain(D):
         m = 1 + t % 2
         pos = a.lengths(m)
         x = torch.from_numpy(np.ascontiguousarray(syn.inputs[t % w.steps][:m])).cuda()
-        if t % 3 == 2:  # a plain step in between: the persistent plan
+        if t % 3 == 2:  # a plain step in between: the persistent plan, equal within rounding
             ya, yb = a.step(x, pos), b.step(x, pos)
-        else:
+            torch.cuda.synchronize()
+            bound = 2e-3 * float(yb.abs().max())
+            assert float((ya - yb).abs().max()) <= bound, t
+        else:  # steps with positions take the kernel chain in both contexts: the same bits
             r3 = torch.from_numpy(_rope_pos(rng, m, syn.max_pos)).cuda()
             ya, yb = a.step(x, pos, rope_pos=r3), b.step(x, pos, rope_pos=r3)
-        torch.cuda.synchronize()
-        assert torch.equal(ya, yb), t
+            torch.cuda.synchronize()
+            assert torch.equal(ya, yb), t
     a.sync()
 
 

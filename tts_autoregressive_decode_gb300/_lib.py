@@ -26,7 +26,7 @@ EXPORTS = ("dec_create", "dec_destroy", "dec_last_error", "dec_set_stream", "dec
            "dec_read_tap", "dec_kernels_per_step", "dec_truncate", "dec_launch_stage",
            "dec_gemv", "dec_attention_workspace_bytes", "dec_attention",
            "dec_attention_noalloc", "dec_flow_create", "dec_flow_step", "dec_flow_destroy",
-           "dec_flow_last_error", "dec_flow_kernels_per_step")
+           "dec_flow_last_error", "dec_flow_kernels_per_step", "dec_inject_stall")
 
 
 class DecFlowConfig(C.Structure):
@@ -122,6 +122,7 @@ def load() -> C.CDLL:
         L.dec_read_tap.argtypes = [vp, i32, i32, vp]
         L.dec_kernels_per_step.argtypes = [vp, i32]
         L.dec_truncate.argtypes = [vp, i32, i32]
+        L.dec_inject_stall.argtypes = [vp, i32, i32]
         L.dec_launch_stage.argtypes = [vp, i32, i32, i32, i32]
         L.dec_gemv.argtypes = [i32, vp, i32, i32, vp, i32, vp, vp]
         L.dec_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
@@ -132,7 +133,7 @@ def load() -> C.CDLL:
                   "dec_sync", "dec_read_kv", "dec_read_tap", "dec_gemv", "dec_attention",
                   "dec_attention_noalloc",
                   "dec_truncate", "dec_launch_stage", "dec_prefill", "dec_read_eos",
-                  "dec_set_mrope", "dec_step_mrope", "dec_prefill_mrope"):
+                  "dec_set_mrope", "dec_step_mrope", "dec_prefill_mrope", "dec_inject_stall"):
             getattr(L, f).restype = i32
         L.dec_get_len.restype = i32
         L.dec_kernels_per_step.restype = i32

@@ -47,7 +47,7 @@ struct LayerW {
 
 // A step plan, one per (m, rotary-position buffer): it serves every input/output pair.  The
 // step's input and output pointers are arguments of a few kernel nodes of the captured graph,
-// updated in place when they change: the persistent kernel's single node, or in the multi-kernel
+// updated in place when they change: the streamed kernel's single node, or in the multi-kernel
 // plan the three launches that take them (layer 0's q/k/v GEMV reads x_in, its o-proj adds
 // x_in as the residual, the final kernel writes the output).  exec is null with
 // DEC_FLAG_NO_GRAPH (the kernels are launched with the step's pointers each time).
@@ -56,11 +56,16 @@ struct PlanEntry {
     const float* x_in;       // the pointers the graph's nodes hold now
     float* out;
     const int32_t* rope;     // per-axis rotary positions of the rows (multi-kernel plans), or null
-    StepPhase* phases;       // device, or null (multi-kernel plan)
+    SPhase* phases;          // streamed plan: its phase list (device), or null (multi-kernel plan)
+    char* sbuf;              // streamed plan: its tagged activation buffers and StreamState
+    size_t sbuf_bytes;
+    StreamState* st;
+    unsigned* cnt;           // streamed plan: its per-phase completion counters
+    long long launches;      // streamed plan: launches since sbuf was last cleared
     cudaGraphExec_t exec;
     cudaGraph_t graph;       // the captured graph, owner of the node handles below
-    cudaGraphNode_t node;    // persistent plan: the kernel node
-    cudaKernelNodeParams kp; // its launch parameters (kernelParams points at a StepParams)
+    cudaGraphNode_t node;    // streamed plan: the kernel node
+    cudaKernelNodeParams kp; // its launch parameters (kernelParams points at a StreamParams)
     cudaGraphNode_t io_node[3];       // multi-kernel plan: q/k/v GEMV, o-proj, final kernel
     cudaKernelNodeParams io_kp[3];    // their launch parameters
     GemvParams io_g[2];               // the two GEMVs' captured arguments
@@ -83,7 +88,7 @@ cudaError_t configure_kernels() {
     if (dev < 64 && (done >> dev & 1u)) return cudaSuccess;
     if ((e = gemv_configure()) != cudaSuccess) return e;
     if ((e = attention_configure()) != cudaSuccess) return e;
-    if ((e = step_configure()) != cudaSuccess) return e;
+    if ((e = stream_configure()) != cudaSuccess) return e;
     if (dev < 64) done |= (uint64_t)1 << dev;
     return cudaSuccess;
 }
@@ -111,7 +116,7 @@ struct dec_ctx {
     int slots = 0;          // KV rows per (layer, stream, kv head)
     int qkv_rows = 0;       // rows of the fused q/k/v matrix
     int max_chunks = 0;     // attention chunks per (stream, kv head)
-    int step_grid[3] = {};  // CTAs of the persistent step kernel for m = 1, 2 (0: not used)
+    int step_grid[3] = {};  // CTAs of the streamed step kernel for m = 1, 2 (0: not used)
     char* arena = nullptr;  // weights
     std::vector<LayerW> L;
     const float* final_norm = nullptr;
@@ -128,7 +133,8 @@ struct dec_ctx {
     float *part = nullptr, *part_ml = nullptr;  // attention chunk partials
     int32_t* len_dev = nullptr;
     unsigned* status = nullptr;
-    GridBarrier* gbar = nullptr;  // the persistent kernel's grid barrier
+    int stall_phase = -1;   // dec_inject_stall: the next step's stalled phase and its poll bound
+    int stall_polls = 0;
     float* taps = nullptr;
     float *io_in = nullptr, *io_out = nullptr;
     unsigned* status_host = nullptr;  // pinned
@@ -226,9 +232,11 @@ void destroy_plan(PlanEntry& e) {
     if (e.exec) cudaGraphExecDestroy(e.exec);
     if (e.graph) cudaGraphDestroy(e.graph);
     if (e.phases) cudaFree(e.phases);
+    if (e.sbuf) cudaFree(e.sbuf);
     e.exec = nullptr;
     e.graph = nullptr;
     e.phases = nullptr;
+    e.sbuf = nullptr;
 }
 
 void destroy_plans(dec_ctx* ctx) {
@@ -378,48 +386,175 @@ FinalParams final_params(dec_ctx* ctx, int m, float* out) {
     return f;
 }
 
-// The persistent kernel's phase list of a step (per layer: QKV, attention, merge, o-proj,
-// gate/up, down; then the output rows).  Each CTA starts staging layer 0's K/V chunk in the
-// first phase and layer l+1's in layer l's o-proj phase.  Empty when some GEMV of the plan is
-// not served by the split-K GEMV.
-std::vector<StepPhase> build_phases(dec_ctx* ctx, int m) {
+// The streamed kernel's plan of a step of m rows: its tagged activation buffers (allocated into
+// pe.sbuf, zeroed) and its phase list (per layer: q/k/v, attention with the merge of its
+// partials, o-proj, gate/up, down; then the output rows).  Layer 0 reads the step input, which
+// is a kernel argument.
+cudaError_t build_stream_plan(dec_ctx* ctx, int m, PlanEntry& pe, std::vector<SPhase>& ph) {
     const dec_config& c = ctx->cfg;
-    std::vector<StepPhase> ph;
-    ph.reserve((size_t)6 * c.layers + 1);
+    const bool talker = c.kind == DEC_QWEN3_TALKER;
+    const int h = c.hidden, d = c.head_dim, H = c.q_heads, G = c.kv_heads, I = c.inter;
+    const int qw = H * d, P = ctx->step_grid[m];
+    const size_t kv_layer = (size_t)ctx->S * G * ctx->slots * d;
+    size_t tot = 0;
+    auto take = [&](size_t words) {
+        const size_t o = tot;
+        tot += align_up(words * sizeof(uint64_t));
+        return o;
+    };
+    const size_t o_qkv = take((size_t)m * ctx->qkv_rows), o_att = take((size_t)m * qw);
+    const size_t o_mid = take((size_t)m * h), o_act = take((size_t)m * I), o_res = take((size_t)m * h);
+    const size_t o_part = take((size_t)m * H * P * d), o_ml = take((size_t)m * H * P * 2);
+    const size_t o_st = tot;
+    tot += align_up(sizeof(StreamState));
+    const size_t o_cnt = tot;
+    tot += align_up((size_t)(5 * c.layers + 1) * sizeof(unsigned));
+    const size_t o_arr = tot;
+    tot += align_up((size_t)c.layers * m * G * sizeof(unsigned));
+    cudaError_t e = cudaMalloc(&pe.sbuf, tot);
+    if (e != cudaSuccess) return e;
+    pe.sbuf_bytes = tot;
+    // (on the context's stream: the plan's first launch is ordered after the clear)
+    if ((e = cudaMemsetAsync(pe.sbuf, 0, tot, ctx->stream)) != cudaSuccess) return e;
+    auto buf = [&](size_t o) { return reinterpret_cast<uint64_t*>(pe.sbuf + o); };
+    uint64_t *qkv = buf(o_qkv), *att = buf(o_att), *mid = buf(o_mid), *act = buf(o_act),
+             *res = buf(o_res), *part = buf(o_part), *ml = buf(o_ml);
+    pe.st = reinterpret_cast<StreamState*>(pe.sbuf + o_st);
+    pe.cnt = reinterpret_cast<unsigned*>(pe.sbuf + o_cnt);
+    unsigned* arr = reinterpret_cast<unsigned*>(pe.sbuf + o_arr);
+    const int es = c.weight_dtype == DEC_BF16 ? 2 : 4, vec = c.weight_dtype == DEC_BF16 ? 8 : 4;
+    auto nj = [&](int K) { return (K / vec + 255) / 256; };
+
+    ph.clear();
     for (int l = 0; l < c.layers; ++l) {
-        for (int stage = 0; stage < 5; ++stage) {
-            StepPhase p = {};
-            p.stage_attn = -1;
-            // layer 0 reads the step input: its pointer is a kernel argument (StepIo)
-            if (l == 0 && stage == 0) p.io = IO_X;
-            if (l == 0 && stage == 2) p.io = IO_RES;
-            if (stage_params(ctx, l, stage, m, nullptr, p.g, p.a)) {
-                p.type = PH_ATTN;
-                ph.push_back(p);
-                p.type = PH_MERGE;
-                ph.push_back(p);
-                continue;
-            }
-            p.type = PH_GEMV;
-            p.nj = rows_gemv_nj(p.g.K, m, c.weight_dtype);
-            if (!p.nj) return {};
-            if (stage == 0 && l == 0) p.stage_attn = 1;
-            if (stage == 2 && l + 1 < c.layers) p.stage_attn = 6 * (l + 1) + 1;
-            ph.push_back(p);
-        }
+        const LayerW& W = ctx->L[l];
+        SPhase p = {};
+        // norm + q/k/v
+        p.type = SP_GEMV;
+        SGemv& g = p.g;
+        g.W = talker ? W.qkv : W.in_proj;
+        g.N = ctx->qkv_rows;
+        g.K = h;
+        g.unit = 1;
+        g.pro = talker ? PRO_RMS : PRO_LN;
+        g.nw = talker ? W.in_norm : W.ln1_w;
+        g.nb = talker ? nullptr : W.ln1_b;
+        g.eps = c.norm_eps;
+        g.epi = EPI_STORE;
+        g.x = l == 0 ? nullptr : res;
+        g.ldx = h;
+        g.x_layer = l - 1;
+        g.y = qkv;
+        g.ldy = ctx->qkv_rows;
+        g.layer = l;
+        p.nj = nj(g.K);
+        ph.push_back(p);
+        // attention, then the merge of its partials
+        p = {};
+        p.type = SP_ATTN;
+        SAttn& a = p.a;
+        a.mode = talker ? ATTN_TALKER : ATTN_RING;
+        a.H = H;
+        a.G = G;
+        a.slots = ctx->slots;
+        a.window = c.window;
+        a.layer = l;
+        a.qkv = qkv;
+        a.ldqkv = ctx->qkv_rows;
+        a.kc = ctx->kc + (size_t)l * kv_layer;
+        a.vc = ctx->vc + (size_t)l * kv_layer;
+        a.pr = talker ? nullptr : ctx->pr + (size_t)l * ctx->S * ctx->slots;
+        a.qn = W.q_norm;
+        a.kn = W.k_norm;
+        a.eps = c.norm_eps;
+        a.rope_cos = ctx->rope_cos;
+        a.rope_sin = ctx->rope_sin;
+        a.part = part;
+        a.ml = ml;
+        a.out = att;
+        a.arr = arr + (size_t)l * m * G;
+        ph.push_back(p);
+        // o-proj + residual (codec: LayerScale)
+        p = {};
+        p.type = SP_GEMV;
+        g = SGemv{};
+        g.W = talker ? W.o : W.out_proj;
+        g.N = h;
+        g.K = qw;
+        g.unit = 1;
+        g.pro = PRO_NONE;
+        g.epi = EPI_RESID;
+        g.ls = talker ? nullptr : W.ls1;
+        g.x = att;
+        g.ldx = qw;
+        g.x_layer = l;
+        g.res = l == 0 ? nullptr : res;
+        g.ldres = h;
+        g.res_layer = l - 1;
+        g.y = mid;
+        g.ldy = h;
+        g.layer = l;
+        p.nj = nj(g.K);
+        ph.push_back(p);
+        // norm + gate/up + SwiGLU (codec: lin1 + GELU)
+        p = {};
+        p.type = SP_GEMV;
+        g = SGemv{};
+        g.W = talker ? W.gu : W.lin1;
+        g.N = talker ? 2 * I : I;
+        g.K = h;
+        g.unit = talker ? 2 : 1;
+        g.pro = talker ? PRO_RMS : PRO_LN;
+        g.nw = talker ? W.post_norm : W.ln2_w;
+        g.nb = talker ? nullptr : W.ln2_b;
+        g.eps = c.norm_eps;
+        g.epi = talker ? EPI_SWIGLU : EPI_GELU;
+        g.x = mid;
+        g.ldx = h;
+        g.x_layer = l;
+        g.y = act;
+        g.ldy = I;
+        g.layer = l;
+        p.nj = nj(g.K);
+        ph.push_back(p);
+        // down + residual (codec: lin2 + LayerScale)
+        p = {};
+        p.type = SP_GEMV;
+        g = SGemv{};
+        g.W = talker ? W.down : W.lin2;
+        g.N = h;
+        g.K = I;
+        g.unit = 1;
+        g.pro = PRO_NONE;
+        g.epi = EPI_RESID;
+        g.ls = talker ? nullptr : W.ls2;
+        g.x = act;
+        g.ldx = I;
+        g.x_layer = l;
+        g.res = mid;
+        g.ldres = h;
+        g.res_layer = l;
+        g.y = res;
+        g.ldy = h;
+        g.layer = l;
+        g.tap = ctx->taps ? ctx->taps + (size_t)l * ctx->S * h : nullptr;
+        g.ldtap = h;
+        p.nj = nj(g.K);
+        ph.push_back(p);
     }
-    for (StepPhase& p : ph)
-        if (p.stage_attn >= 0) {
-            p.stage_kc = ph[p.stage_attn].a.kc;
-            p.stage_vc = ph[p.stage_attn].a.vc;
-        }
-    StepPhase f = {};
-    f.type = PH_FINAL;
-    f.stage_attn = -1;
-    f.io = IO_OUT;
-    f.f = final_params(ctx, m, nullptr);
+    SPhase f = {};
+    f.type = SP_FINAL;
+    f.f.x = res;
+    f.f.layer = c.layers - 1;
+    f.f.h = h;
+    f.f.w = ctx->final_norm;
+    f.f.b = ctx->final_norm_b;
+    f.f.eos_w = ctx->eos_w;
+    f.f.eos = ctx->eos;
+    f.f.eps = c.norm_eps;
     ph.push_back(f);
-    return ph;
+    (void)es;
+    return cudaSuccess;
 }
 
 // The graph node the last launch captured on `s` became (null when `s` is not capturing).
@@ -491,15 +626,21 @@ cudaError_t update_io_nodes(PlanEntry& pe, const float* x_in, float* out) {
     return cudaSuccess;
 }
 
-StepParams step_params(dec_ctx* ctx, const StepPhase* phases, const float* x_in, float* out) {
-    StepParams sp = {};
-    sp.phases = phases;
-    sp.n_phases = 6 * ctx->cfg.layers + 1;
-    sp.attn0 = 1;
-    sp.bar = ctx->gbar;
-    sp.status = ctx->status;
+StreamParams stream_params(dec_ctx* ctx, const PlanEntry& pe, const float* x_in, float* out,
+                           int stall_phase = -1, int stall_polls = 0) {
+    StreamParams sp = {};
+    sp.phases = pe.phases;
+    sp.n_phases = 5 * ctx->cfg.layers + 1;
+    sp.m = pe.m;
     sp.x_in = x_in;
     sp.out = out;
+    sp.len = ctx->len_dev;
+    sp.max_pos = ctx->cfg.max_pos;
+    sp.st = pe.st;
+    sp.cnt = pe.cnt;
+    sp.status = ctx->status;
+    sp.wait_polls = stall_polls;
+    sp.stall_phase = stall_phase;
     return sp;
 }
 
@@ -534,17 +675,28 @@ cudaError_t enqueue_prefill_block(dec_ctx* ctx, int stream, int m, const float* 
     return launch_final(f, s, true);
 }
 
-// Enqueue one step of a plan: the persistent kernel when the plan has a phase list, else the
+// Enqueue one step of a plan: the streamed kernel when the plan has a phase list, else the
 // kernels one by one.
 cudaError_t enqueue_step(dec_ctx* ctx, PlanEntry& pe, const float* x_in, float* out,
-                         cudaStream_t s, bool record = false) {
+                         cudaStream_t s, bool record = false, int stall_phase = -1,
+                         int stall_polls = 0) {
     if (!pe.phases) return enqueue_kernels(ctx, pe.m, x_in, out, s, pe.rope, record ? &pe : nullptr);
-    return launch_step(step_params(ctx, pe.phases, x_in, out), ctx->cfg.weight_dtype, pe.m,
-                       ctx->cfg.head_dim, ctx->step_grid[pe.m], s);
+    return launch_stream_step(stream_params(ctx, pe, x_in, out, stall_phase, stall_polls),
+                              ctx->cfg.weight_dtype, pe.m, ctx->cfg.head_dim, ctx->step_grid[pe.m], s);
 }
 
-bool uses_persistent(const dec_ctx* ctx, int m) {
-    return m >= 1 && m <= 2 && ctx->step_grid[m] > 0;
+// Whether steps of m rows take the streamed kernel: m <= 2, the kernel launchable here, and
+// every GEMV, head group and output row within its limits.
+bool uses_stream(const dec_ctx* ctx, int m) {
+    if (m < 1 || m > 2 || ctx->step_grid[m] <= 0) return false;
+    const dec_config& c = ctx->cfg;
+    const int dt = c.weight_dtype;
+    // the attention key split is 32-bit: keys of all streams and kv heads times (grid + 1)
+    if ((uint64_t)m * c.kv_heads * ctx->slots * (uint64_t)(ctx->step_grid[m] + 1) >= (1ull << 32))
+        return false;
+    return c.layers <= kStreamMaxLayers && c.hidden <= 8192 && c.q_heads / c.kv_heads <= kMaxGroup &&
+           stream_gemv_ok(dt, c.hidden) && stream_gemv_ok(dt, c.inter) &&
+           stream_gemv_ok(dt, c.q_heads * c.head_dim);
 }
 
 // The plan for (m, x_in, out, rope): found in the cache or built (phase list uploaded, graph
@@ -558,15 +710,17 @@ PlanEntry* get_plan(dec_ctx* ctx, int m, const float* x_in, float* out, const in
     pe.x_in = x_in;
     pe.out = out;
     pe.rope = rope;
-    if (!rope && uses_persistent(ctx, m)) {
-        const std::vector<StepPhase> ph = build_phases(ctx, m);
-        if (!ph.empty()) {
-            const size_t bytes = ph.size() * sizeof(StepPhase);
-            if ((*err = cudaMalloc(&pe.phases, bytes)) != cudaSuccess) return nullptr;
-            if ((*err = cudaMemcpy(pe.phases, ph.data(), bytes, cudaMemcpyHostToDevice)) != cudaSuccess) {
-                destroy_plan(pe);
-                return nullptr;
-            }
+    if (!rope && uses_stream(ctx, m)) {
+        std::vector<SPhase> ph;
+        if ((*err = build_stream_plan(ctx, m, pe, ph)) != cudaSuccess) {
+            destroy_plan(pe);
+            return nullptr;
+        }
+        const size_t bytes = ph.size() * sizeof(SPhase);
+        if ((*err = cudaMalloc(&pe.phases, bytes)) != cudaSuccess ||
+            (*err = cudaMemcpy(pe.phases, ph.data(), bytes, cudaMemcpyHostToDevice)) != cudaSuccess) {
+            destroy_plan(pe);
+            return nullptr;
         }
     }
     if (!(ctx->cfg.flags & DEC_FLAG_NO_GRAPH)) {
@@ -634,7 +788,7 @@ dec_status run_step(dec_ctx* ctx, int m, const float* x_in, float* out,
     if (pe->exec && (pe->x_in != x_in || pe->out != out)) {
         // new input/output buffers: update the kernel nodes' arguments in place
         if (pe->phases) {
-            StepParams sp = step_params(ctx, pe->phases, x_in, out);
+            StreamParams sp = stream_params(ctx, *pe, x_in, out);
             void* args[] = {&sp};
             cudaKernelNodeParams kp = pe->kp;
             kp.kernelParams = args;
@@ -651,7 +805,22 @@ dec_status run_step(dec_ctx* ctx, int m, const float* x_in, float* out,
         pe->x_in = x_in;
         pe->out = out;
     }
-    e = pe->exec ? cudaGraphLaunch(pe->exec, ctx->stream) : enqueue_step(ctx, *pe, x_in, out, ctx->stream);
+    if (pe->phases) {
+        // the tags of the streamed plan hold (launches + 1) << 8 in 32 bits: start the buffers
+        // and the count over long before the tag could come round to an old value
+        if (++pe->launches >= (1LL << 22)) {
+            e = cudaMemsetAsync(pe->sbuf, 0, pe->sbuf_bytes, ctx->stream);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "tag reset");
+            pe->launches = 1;
+        }
+    }
+    if (pe->phases && ctx->stall_phase >= 0) {
+        // dec_inject_stall: this one step runs outside the graph with its stalled phase
+        e = enqueue_step(ctx, *pe, x_in, out, ctx->stream, false, ctx->stall_phase, ctx->stall_polls);
+        ctx->stall_phase = -1;
+    } else {
+        e = pe->exec ? cudaGraphLaunch(pe->exec, ctx->stream) : enqueue_step(ctx, *pe, x_in, out, ctx->stream);
+    }
     if (e != cudaSuccess) return cuda_fail(ctx, e, "step launch");
     for (int i = 0; i < m; ++i) ctx->len_host[i] += 1;
     return DEC_OK;
@@ -662,8 +831,6 @@ dec_status read_status(dec_ctx* ctx) {
     if (st == 0) return DEC_OK;
     *ctx->status_host = 0;
     cudaMemset(ctx->status, 0, sizeof(unsigned));
-    // a barrier wait that gave up leaves the grid barrier mid-count: start it over (nothing runs)
-    if ((st & CHECK_WAIT_LIMIT) && ctx->gbar) cudaMemset(ctx->gbar, 0, sizeof(GridBarrier));
     return fail(ctx, DEC_E_DEVICE_CHECK, "device check fired:%s%s",
                 (st & CHECK_WAIT_LIMIT) ? " wait-limit" : "", (st & CHECK_BOUNDS) ? " bounds" : "");
 }
@@ -730,7 +897,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->max_chunks = (ctx->slots + kAttnChunk - 1) / kAttnChunk;
     if (c.flags & DEC_FLAG_PERSISTENT)
         for (int mm = 1; mm <= std::min(2, ctx->S); ++mm)
-            ctx->step_grid[mm] = step_grid(c.weight_dtype, mm, d, ctx->num_sms);
+            ctx->step_grid[mm] = stream_grid(c.weight_dtype, mm, d, ctx->num_sms);
     e = cudaStreamCreateWithFlags(&ctx->cap_stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "capture stream"));
     if ((e = cudaMallocHost(&ctx->status_host, sizeof(unsigned))) != cudaSuccess)
@@ -862,7 +1029,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     const size_t o_att = take((size_t)R * qw * 4), o_act = take((size_t)R * I * 4);
     const size_t o_part = take(attention_part_bytes(R, H, ctx->max_chunks, d));
     const size_t o_ml = take(attention_ml_bytes(R, H, ctx->max_chunks));
-    const size_t o_len = take((size_t)S * 4), o_st = take(4), o_gbar = take(sizeof(GridBarrier));
+    const size_t o_len = take((size_t)S * 4), o_st = take(4);
     const size_t o_eos = take((size_t)S * 4);
     const size_t o_taps = (c.flags & DEC_FLAG_TAPS) ? take((size_t)c.layers * S * h * 4) : 0;
     const size_t o_in = take((size_t)S * h * 4), o_out = take((size_t)S * h * 4);
@@ -882,7 +1049,6 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->part_ml = reinterpret_cast<float*>(b + o_ml);
     ctx->len_dev = reinterpret_cast<int32_t*>(b + o_len);
     ctx->status = reinterpret_cast<unsigned*>(b + o_st);
-    ctx->gbar = reinterpret_cast<GridBarrier*>(b + o_gbar);
     ctx->eos = reinterpret_cast<float*>(b + o_eos);
     ctx->taps = (c.flags & DEC_FLAG_TAPS) ? reinterpret_cast<float*>(b + o_taps) : nullptr;
     ctx->io_in = reinterpret_cast<float*>(b + o_in);
@@ -1125,13 +1291,19 @@ dec_status dec_read_tap(dec_ctx* ctx, int layer, int m, float* dst_host) {
 
 int dec_kernels_per_step(const dec_ctx* ctx, int m) {
     if (!ctx || m < 1 || m > ctx->S) return -1;
-    if (uses_persistent(ctx, m)) {
-        // the persistent kernel serves the plan unless one of its GEMVs is too wide for it
-        const int wide = std::max(std::max(ctx->cfg.hidden, ctx->cfg.inter),
-                                  ctx->cfg.q_heads * ctx->cfg.head_dim);
-        if (rows_gemv_nj(wide, m, ctx->cfg.weight_dtype)) return 1;
-    }
+    if (uses_stream(ctx, m)) return 1;
     return 6 * ctx->cfg.layers + 1;
+}
+
+dec_status dec_inject_stall(dec_ctx* ctx, int phase, int polls) {
+    if (!ctx) return fail(nullptr, DEC_E_ARG, "ctx is NULL");
+    if (ctx->step_grid[1] <= 0 && ctx->step_grid[2] <= 0)
+        return fail(ctx, DEC_E_UNSUPPORTED, "the context has no persistent plan");
+    if (phase < 0 || phase > 5 * ctx->cfg.layers || polls < 1)
+        return fail(ctx, DEC_E_ARG, "phase %d outside 0..%d or polls < 1", phase, 5 * ctx->cfg.layers);
+    ctx->stall_phase = phase;
+    ctx->stall_polls = polls;
+    return DEC_OK;
 }
 
 dec_status dec_truncate(dec_ctx* ctx, int stream, int new_len) {

@@ -150,52 +150,109 @@ struct FinalParams {
 cudaError_t launch_final(const FinalParams& p, cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------------------------------------
-// Persistent step kernel (m <= 2): the step's phases run in one cooperative launch, separated by
-// grid-wide barriers.  A phase is one GEMV, the attention chunks, their merge, or the output rows.
+// Streamed step kernel (m <= 2 rows): the whole step as one persistent cooperative launch, one
+// CTA per SM.  Per CTA a producer warp streams the CTA's share of every phase's weights and K/V
+// rows through a shared-memory ring by bulk copies, running ahead across phase boundaries; the
+// consumer warps compute each phase once its input activations are there.  Activations travel
+// between CTAs as tagged words: the low half is the f32 value, the high half the tag of the
+// (launch, layer) that wrote it, so waiting for an input and reading it are one load.
 // ---------------------------------------------------------------------------------------------
-enum PhaseType : int { PH_GEMV = 0, PH_ATTN = 1, PH_MERGE = 2, PH_FINAL = 3 };
-// The step's input and output pointers are kernel arguments, not part of the phase list, so one
-// list (and one captured graph) serves every input/output buffer pair.
-enum StepIo : int { IO_X = 1, IO_RES = 2, IO_OUT = 4 };  // g.x, g.res := x_in; f.out := out
+enum StreamPhaseType : int { SP_GEMV = 0, SP_ATTN = 1, SP_FINAL = 3 };
 
-struct StepPhase {
-    int type;              // PhaseType
-    int nj;                // PH_GEMV: 16-byte weight granules per lane (1..4)
-    int stage_attn;        // index of a later PH_ATTN phase whose K/V chunk each CTA starts
-                           // staging into shared memory when this phase begins (-1: none)
-    int io;                // StepIo bits: fields that take the launch's input / output pointer
-    const float* stage_kc; // stage_attn >= 0: that phase's K and V caches
-    const float* stage_vc;
-    GemvParams g;          // PH_GEMV
-    AttnParams a;          // PH_ATTN, PH_MERGE
-    FinalParams f;         // PH_FINAL
+struct SGemv {
+    const void* W;
+    int N, K;
+    int unit;               // rows per partition unit (2: SwiGLU gate/up pairs)
+    int pro;                // PRO_NONE / PRO_RMS / PRO_LN
+    const float* nw;        // norm weight [K]
+    const float* nb;        // LayerNorm bias [K]
+    float eps;
+    int epi;                // EPI_STORE / EPI_RESID / EPI_SWIGLU / EPI_GELU
+    const float* ls;        // LayerScale [N] or null (EPI_RESID)
+    const uint64_t* x;      // tagged input [m][ldx] written at layer x_layer; null: the step input
+    int ldx, x_layer;
+    const uint64_t* res;    // tagged residual [m][ldres] at layer res_layer; null: the step input
+    int ldres, res_layer;
+    uint64_t* y;            // tagged output [m][ldy], written with tag `layer`
+    int ldy, layer;
+    float* tap;             // optional plain copy of the EPI_RESID output [m][ldtap]
+    int ldtap;
 };
 
-// Grid barrier of the persistent kernel: `count` only grows (mod 2^32), by one per CTA and
-// barrier; barrier k of a launch completes when count reaches base + (k + 1) * grid.  `base` is
-// the count at the start of a launch, written by CTA 0 after the launch's last barrier.  Both
-// start at zero (and are zeroed again after a wait gave up).
-struct GridBarrier {
-    unsigned count;
-    unsigned base;
+struct SAttn {
+    int mode;               // ATTN_TALKER or ATTN_RING
+    int H, G;
+    int slots, window;
+    int layer;              // tag of the q/k/v rows read and of the partials written
+    const uint64_t* qkv;    // tagged raw [m][ldqkv] = [q | k | v]
+    int ldqkv;
+    float* kc;              // K cache [m][G][slots][d] (this layer)
+    float* vc;
+    uint32_t* pr;           // RING: position stamps [m][slots]
+    const float* qn;        // TALKER: q / k norm weights [d]
+    const float* kn;
+    float eps;
+    const float* rope_cos;  // [max_pos][d/2]
+    const float* rope_sin;
+    uint64_t* part;         // tagged partial outputs [m][H][grid][d]
+    uint64_t* ml;           // tagged partial (max, sum) [m][H][grid][2]
+    uint64_t* out;          // tagged attention output [m][H * d] (merged partials)
+    unsigned* arr;          // [m][G] arrival counts of this layer's (stream, kv head) pairs,
+                            // zero between launches
 };
 
-struct StepParams {
-    const StepPhase* phases;  // device array
+struct SFinal {
+    const uint64_t* x;      // tagged residual stream [m][h] of layer `layer`
+    int layer, h;
+    const float* w;         // RMSNorm weight (talker), LayerNorm weight (codec head), or null
+    const float* b;         // LayerNorm bias (codec head) or null
+    const float* eos_w;     // EOS row [h] or null
+    float* eos;             // [m]
+    float eps;
+};
+
+struct SPhase {
+    int type;               // StreamPhaseType
+    int nj;                 // SP_GEMV: 16-byte granules of a row per consumer thread (1..4)
+    SGemv g;
+    SAttn a;
+    SFinal f;
+};
+
+// Per-plan device state: `epoch` counts the plan's launches (tags are (epoch + 1) << 8 | layer),
+// `exit_count` the CTAs that have finished the current launch.
+struct StreamState {
+    unsigned epoch;
+    unsigned exit_count;
+};
+
+struct StreamParams {
+    const SPhase* phases;   // device array
     int n_phases;
-    int attn0;                // index of the first PH_ATTN phase (-1: none)
-    const float* x_in;        // the step's input rows [m][hidden]
-    float* out;               // the step's output rows [m][hidden]
-    GridBarrier* bar;
-    unsigned* status;
+    int m;                  // rows (streams 0..m-1)
+    const float* x_in;      // the step's input rows [m][hidden]
+    float* out;             // the step's output rows [m][hidden]
+    int32_t* len;           // [m] stream lengths: read at the start, advanced at the end
+    int max_pos;            // rows of the rope tables
+    StreamState* st;
+    unsigned* cnt;          // [n_phases] completion counters: each CTA adds 1 when its part of the
+                            // phase is written; phase i + 1 starts once cnt[i] = (epoch + 1) * grid
+    unsigned* status;       // device check word
+    int wait_polls;         // bound on the polls of one wait (0: the default bound)
+    int stall_phase;        // -1; else the consumers of this phase wait for a tag that no CTA
+                            // writes, so the wait runs out (tests of the bounded waits)
 };
 
-// CTAs of the persistent kernel on this device for the given weight dtype, rows and head_dim
-// (2 per SM when they fit, else 1; 0 when a cooperative launch is not possible).
-int step_grid(int dtype, int m, int d, int num_sms);
-cudaError_t step_configure();
-// One step: a cooperative launch of `grid` CTAs (grid = step_grid(...)).
-cudaError_t launch_step(const StepParams& sp, int dtype, int m, int d, int grid, cudaStream_t s);
+// Layers the tag scheme takes.
+constexpr int kStreamMaxLayers = 255;
+// CTAs of the streamed kernel on this device (one per SM; 0 when it cannot be launched).
+int stream_grid(int dtype, int m, int d, int num_sms);
+cudaError_t stream_configure();
+// Whether a GEMV of K columns fits the kernel (a row within one ring slot, at most 4 granules
+// per consumer thread).
+bool stream_gemv_ok(int dtype, int K);
+cudaError_t launch_stream_step(const StreamParams& sp, int dtype, int m, int d, int grid,
+                               cudaStream_t s);
 
 struct PrefillParams {
     int layers, n, G, d, slots, streams, stream;

@@ -224,6 +224,11 @@ class Decoder:
     def kernels_per_step(self, m: int) -> int:
         return int(self.lib.dec_kernels_per_step(self.h, m))
 
+    def inject_stall(self, phase: int, polls: int) -> None:
+        """The next persistent-plan step waits in `phase` for activations no CTA writes, each
+        wait bounded by `polls` loads (dec_inject_stall): a check of the bounded-wait path."""
+        L.check(self.lib.dec_inject_stall(self.h, int(phase), int(polls)), self.h)
+
     def truncate(self, stream: int, new_len: int) -> None:
         L.check(self.lib.dec_truncate(self.h, stream, new_len), self.h)
 

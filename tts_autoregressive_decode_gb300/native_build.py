@@ -4,6 +4,7 @@ Each CUDA translation unit is compiled in parallel with one -gencode (compute_10
 then linked into a shared library with the CUDA runtime linked statically.  ptxas resource
 lines (registers, spills, shared memory) go to _build/ptxas.log.
 """
+import fcntl
 import os
 import shutil
 import subprocess
@@ -15,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libttsdec.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["step.cu", "gemv.cu", "attention.cu", "misc.cu", "dec_api.cu", "flow_api.cu",
+SOURCES = ["stream_step.cu", "gemv.cu", "attention.cu", "misc.cu", "dec_api.cu", "flow_api.cu",
            "noalloc.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -44,6 +45,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    # one build at a time (test workers may start it together); the others wait, then find the
+    # library fresh
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not stale():
+            return LIB
+        return _build(verbose)
+
+
+def _build(verbose: bool) -> str:
     cc = nvcc()
     flags = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
              "-I", INCLUDE]
