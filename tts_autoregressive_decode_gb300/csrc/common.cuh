@@ -83,6 +83,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// 1-D bulk copy global -> shared with an L2 policy (weights, cached K/V: evict_first)
+__device__ __forceinline__ void bulk_g2s_pol(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 // ---- L2 cache policy -----------------------------------------------------------------------
 // evict_first: data streamed once (weights), so it does not push out data that is reused
 __device__ __forceinline__ uint64_t l2_evict_first() {

@@ -1,5 +1,5 @@
 // gemv_rows.cuh -- the split-K row-streaming GEMV for m <= 8 rows as device functions, shared by
-// the stand-alone kernel (gemv.cu) and the persistent step kernel (step.cu, m <= 2).
+// the stand-alone kernel (gemv.cu) and its callers.
 //
 // y[r][n] = sum_k W[n][k] xin[r][k]; W row-major [N][K] (Qwen3-TTS talker on wgpu, MATVEC_SRC:
 // each weight is read once for all rows), f32 or bf16 bit patterns widened exactly.
@@ -15,8 +15,8 @@
 // (lanes 4r..4r+3 end up holding row r); the cross-warp sum and the epilogue run once per
 // segment of at most kRowsMaxRows rows.
 //
-// Activations (x, the residual) are read with ld.global.cg: inside the persistent kernel they
-// were written by other CTAs of the same launch, so they must not come from a stale L1 line.
+// Activations (x, the residual) are read with ld.global.cg (L2): they were written by the
+// previous kernel of the chain, on other SMs.
 #pragma once
 
 #include "common.cuh"
@@ -122,252 +122,277 @@ struct RowsGemv {
         load(p, Wb, row_bytes, RB, lim, pol, wb);
     }
 
-    // everything after issue(): x and the norm prologue, the remaining batches, the epilogue.
-    // Every thread of the CTA calls it (block-wide barriers inside).
-    __device__ static void run(const GemvParams& p, int b, int P, uint4 (&wa)[BUF],
-                               uint4 (&wb)[BUF], float* sh) {
-        float* red = sh;                                          // [warps][kRowsMaxRows][MT]
-        float* nred = red + kRowsWarps * kRowsMaxRows * MT;       // [warps][MT]
-        float* stat = nred + kRowsWarps * MT;                     // [2][MT]
-        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-        const int K = p.K, m = p.m;
-        const int G = K / VEC;
+    // A thread's share of one CTA's rows: the row range, its weight granules, its slice of x
+    // (normalised in place by the prologue) and its prefetched residual-epilogue operands.
+    struct Lane {
         int row0, nrows;
-        range(p, b, P, row0, nrows);
-        const size_t row_bytes = (size_t)K * ES;
-        const char* Wb = static_cast<const char*>(p.W) + (size_t)row0 * row_bytes;
-        const uint64_t pol = l2_evict_first();
-
         int gj[NJ];
         bool ok[NJ];
+        float2 xv[MT][NJ][VEC / 2];
+        float res_v, ls_v, bias_v;
+    };
+
+    // The residual epilogue's operands of this thread's output (row tid / m, stream tid % m),
+    // fetched together with x rather than after the rows are summed.  With m <= 2 a segment
+    // has at most kRowsMaxRows * 2 <= kRowsThreads outputs, one per thread; wider rows read
+    // them in the epilogue's loop instead.
+    static constexpr bool kEpiPrefetch = MT <= 2;
+
+    __device__ static void setup(const GemvParams& p, int b, int P, Lane& L) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        range(p, b, P, L.row0, L.nrows);
+        const int G = p.K / VEC;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
-            gj[j] = (j * kRowsWarps + warp) * 32 + lane;
-            ok[j] = gj[j] < G;
+            L.gj[j] = (j * kRowsWarps + warp) * 32 + lane;
+            L.ok[j] = L.gj[j] < G;
         }
+        L.res_v = L.ls_v = L.bias_v = 0.f;
+    }
 
-        // The residual epilogue's operands of this thread's output (row tid / m, stream tid % m),
-        // fetched together with x rather than after the rows are summed.  With m <= 2 a segment
-        // has at most kRowsMaxRows * 2 <= kRowsThreads outputs, one per thread; wider rows read
-        // them in the epilogue's loop instead.
-        constexpr bool kEpiPrefetch = MT <= 2;
-        float res_v = 0.f, ls_v = 0.f, bias_v = 0.f;
-        auto fetch_epi = [&](int seg) {
-            if constexpr (!kEpiPrefetch) return;
-            const int srows = nrows - seg < kRowsMaxRows ? nrows - seg : kRowsMaxRows;
-            if (tid < srows * m) {
-                const int row = row0 + seg + tid / m, mm = tid % m;
-                if (p.bias) bias_v = p.bias[row];
-                if (p.epi == EPI_RESID) {
-                    res_v = __ldcg(p.res + (size_t)mm * p.ldres + row);
-                    if (p.ls) ls_v = __ldcg(p.ls + row);
-                }
+    __device__ static void fetch_epi(const GemvParams& p, Lane& L, int seg) {
+        if constexpr (!kEpiPrefetch) return;
+        const int tid = threadIdx.x, m = p.m;
+        const int srows = L.nrows - seg < kRowsMaxRows ? L.nrows - seg : kRowsMaxRows;
+        if (tid < srows * m) {
+            const int row = L.row0 + seg + tid / m, mm = tid % m;
+            if (p.bias) L.bias_v = p.bias[row];
+            if (p.epi == EPI_RESID) {
+                L.res_v = __ldcg(p.res + (size_t)mm * p.ldres + row);
+                if (p.ls) L.ls_v = __ldcg(p.ls + row);
             }
-        };
-        if (nrows > 0) fetch_epi(0);
+        }
+    }
 
-        // ---- x slice in registers, norm prologue as a block reduction -----------------------
-        float2 xv[MT][NJ][VEC / 2];
+    // x slice into registers, then the norm prologue (a block reduction).  Every thread of the
+    // CTA calls it (block-wide barriers inside).
+    __device__ static void prologue(const GemvParams& p, Lane& L, float* sh) {
+        float* nred = sh + kRowsWarps * kRowsMaxRows * MT;  // [warps][MT]
+        float* stat = nred + kRowsWarps * MT;               // [2][MT]
+        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        const int K = p.K, m = p.m;
 #pragma unroll
         for (int mm = 0; mm < MT; ++mm)
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
-                const float* src = p.x + (size_t)mm * p.ldx + (size_t)gj[j] * VEC;
+                const float* src = p.x + (size_t)mm * p.ldx + (size_t)L.gj[j] * VEC;
 #pragma unroll
                 for (int q = 0; q < VEC / 4; ++q) {
                     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (mm < m && ok[j]) a = __ldcg(reinterpret_cast<const float4*>(src + 4 * q));
-                    xv[mm][j][2 * q] = make_float2(a.x, a.y);
-                    xv[mm][j][2 * q + 1] = make_float2(a.z, a.w);
+                    if (mm < m && L.ok[j]) a = __ldcg(reinterpret_cast<const float4*>(src + 4 * q));
+                    L.xv[mm][j][2 * q] = make_float2(a.x, a.y);
+                    L.xv[mm][j][2 * q + 1] = make_float2(a.z, a.w);
                 }
             }
-        if (p.pro != PRO_NONE) {
-            auto block_sum = [&](float (&v)[MT], int slot) {
-#pragma unroll
-                for (int mm = 0; mm < MT; ++mm) {
-                    const float t = warp_sum(v[mm]);
-                    if (lane == 0) nred[warp * MT + mm] = t;
-                }
-                __syncthreads();
-                if (tid < MT) {
-                    float sum = 0.f;
-                    for (int w = 0; w < kRowsWarps; ++w) sum += nred[w * MT + tid];
-                    stat[slot * MT + tid] = sum / (float)K;
-                }
-                __syncthreads();
-            };
-            float part[MT];
+        if (p.pro == PRO_NONE) return;
+        auto block_sum = [&](float (&v)[MT], int slot) {
 #pragma unroll
             for (int mm = 0; mm < MT; ++mm) {
+                const float t = warp_sum(v[mm]);
+                if (lane == 0) nred[warp * MT + mm] = t;
+            }
+            __syncthreads();
+            if (tid < MT) {
+                float sum = 0.f;
+                for (int w = 0; w < kRowsWarps; ++w) sum += nred[w * MT + tid];
+                stat[slot * MT + tid] = sum / (float)K;
+            }
+            __syncthreads();
+        };
+        float part[MT];
+#pragma unroll
+        for (int mm = 0; mm < MT; ++mm) {
+            part[mm] = 0.f;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+#pragma unroll
+                for (int e = 0; e < VEC / 2; ++e) {
+                    const float2 v = L.xv[mm][j][e];
+                    part[mm] += (p.pro != PRO_RMS) ? v.x + v.y : v.x * v.x + v.y * v.y;
+                }
+        }
+        block_sum(part, 0);  // mean (LayerNorm) or mean square (RMSNorm)
+        float inv[MT], mean[MT];
+        if (p.pro != PRO_RMS) {
+#pragma unroll
+            for (int mm = 0; mm < MT; ++mm) {
+                mean[mm] = stat[mm];
                 part[mm] = 0.f;
 #pragma unroll
                 for (int j = 0; j < NJ; ++j)
 #pragma unroll
                     for (int e = 0; e < VEC / 2; ++e) {
-                        const float2 v = xv[mm][j][e];
-                        part[mm] += (p.pro != PRO_RMS) ? v.x + v.y : v.x * v.x + v.y * v.y;
+                        if (!L.ok[j]) continue;
+                        const float dx = L.xv[mm][j][e].x - mean[mm], dy = L.xv[mm][j][e].y - mean[mm];
+                        part[mm] += dx * dx + dy * dy;
                     }
             }
-            block_sum(part, 0);  // mean (LayerNorm) or mean square (RMSNorm)
-            float inv[MT], mean[MT];
-            if (p.pro != PRO_RMS) {
+            block_sum(part, 1);
 #pragma unroll
-                for (int mm = 0; mm < MT; ++mm) {
-                    mean[mm] = stat[mm];
-                    part[mm] = 0.f;
+            for (int mm = 0; mm < MT; ++mm) inv[mm] = 1.0f / sqrtf(stat[MT + mm] + p.eps);
+        } else {
 #pragma unroll
-                    for (int j = 0; j < NJ; ++j)
-#pragma unroll
-                        for (int e = 0; e < VEC / 2; ++e) {
-                            if (!ok[j]) continue;
-                            const float dx = xv[mm][j][e].x - mean[mm], dy = xv[mm][j][e].y - mean[mm];
-                            part[mm] += dx * dx + dy * dy;
-                        }
-                }
-                block_sum(part, 1);
-#pragma unroll
-                for (int mm = 0; mm < MT; ++mm) inv[mm] = 1.0f / sqrtf(stat[MT + mm] + p.eps);
-            } else {
-#pragma unroll
-                for (int mm = 0; mm < MT; ++mm) {
-                    mean[mm] = 0.f;
-                    inv[mm] = 1.0f / sqrtf(stat[mm] + p.eps);
-                }
+            for (int mm = 0; mm < MT; ++mm) {
+                mean[mm] = 0.f;
+                inv[mm] = 1.0f / sqrtf(stat[mm] + p.eps);
             }
+        }
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                if (!ok[j]) continue;
-                const int k0 = gj[j] * VEC;
+        for (int j = 0; j < NJ; ++j) {
+            if (!L.ok[j]) continue;
+            const int k0 = L.gj[j] * VEC;
 #pragma unroll
-                for (int e = 0; e < VEC / 2; ++e) {
-                    // a LayerNorm without affine weights (the flow head's final norm) is w 1, b 0
-                    const float2 w = p.nw ? *reinterpret_cast<const float2*>(p.nw + k0 + 2 * e)
-                                          : make_float2(1.f, 1.f);
-                    float2 bb = make_float2(0.f, 0.f);
-                    if (p.pro != PRO_RMS && p.nb) bb = *reinterpret_cast<const float2*>(p.nb + k0 + 2 * e);
+            for (int e = 0; e < VEC / 2; ++e) {
+                // a LayerNorm without affine weights (the flow head's final norm) is w 1, b 0
+                const float2 w = p.nw ? *reinterpret_cast<const float2*>(p.nw + k0 + 2 * e)
+                                      : make_float2(1.f, 1.f);
+                float2 bb = make_float2(0.f, 0.f);
+                if (p.pro != PRO_RMS && p.nb) bb = *reinterpret_cast<const float2*>(p.nb + k0 + 2 * e);
+#pragma unroll
+                for (int mm = 0; mm < MT; ++mm) {
+                    float2& v = L.xv[mm][j][e];
+                    v.x = (v.x - mean[mm]) * inv[mm] * w.x + bb.x;
+                    v.y = (v.y - mean[mm]) * inv[mm] * w.y + bb.y;
+                }
+                if (p.pro == PRO_LN_MOD) {  // modulate: n (1 + scale) + shift
+                    const float2 sh2 = __ldcg(reinterpret_cast<const float2*>(p.mod + k0 + 2 * e));
+                    const float2 sc = __ldcg(reinterpret_cast<const float2*>(p.mod + K + k0 + 2 * e));
 #pragma unroll
                     for (int mm = 0; mm < MT; ++mm) {
-                        float2& v = xv[mm][j][e];
-                        v.x = (v.x - mean[mm]) * inv[mm] * w.x + bb.x;
-                        v.y = (v.y - mean[mm]) * inv[mm] * w.y + bb.y;
-                    }
-                    if (p.pro == PRO_LN_MOD) {  // modulate: n (1 + scale) + shift
-                        const float2 sh = __ldcg(reinterpret_cast<const float2*>(p.mod + k0 + 2 * e));
-                        const float2 sc = __ldcg(reinterpret_cast<const float2*>(p.mod + K + k0 + 2 * e));
-#pragma unroll
-                        for (int mm = 0; mm < MT; ++mm) {
-                            float2& v = xv[mm][j][e];
-                            v.x = v.x * (1.0f + sc.x) + sh.x;
-                            v.y = v.y * (1.0f + sc.y) + sh.y;
-                        }
+                        float2& v = L.xv[mm][j][e];
+                        v.x = v.x * (1.0f + sc.x) + sh2.x;
+                        v.y = v.y * (1.0f + sc.y) + sh2.y;
                     }
                 }
             }
         }
+    }
 
-        // ---- stream the rows, segment by segment, in double-buffered batches ------------------
-        auto consume = [&](const uint4 (&w)[BUF], int b0, int lim) {
+    // One batch of RB rows (rows b0.. of the segment; rows at or past lim are not stored): the
+    // thread's partial dot products, folded across lanes, into the cross-warp scratch.
+    __device__ static void consume(const uint4 (&w)[BUF], int b0, int lim, const Lane& L,
+                                   float* red) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-            for (int g8 = 0; g8 < RB; g8 += 8) {  // 8 rows per transposed butterfly
-                float part[MT][8];
+        for (int g8 = 0; g8 < RB; g8 += 8) {  // 8 rows per transposed butterfly
+            float part[MT][8];
 #pragma unroll
-                for (int mm = 0; mm < MT; ++mm)
+            for (int mm = 0; mm < MT; ++mm)
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) part[mm][r] = 0.f;
+                for (int r = 0; r < 8; ++r) part[mm][r] = 0.f;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    if (g8 + r >= RB) break;
-                    float2 acc[MT];
+            for (int r = 0; r < 8; ++r) {
+                if (g8 + r >= RB) break;
+                float2 acc[MT];
 #pragma unroll
-                    for (int mm = 0; mm < MT; ++mm) acc[mm] = make_float2(0.f, 0.f);
+                for (int mm = 0; mm < MT; ++mm) acc[mm] = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < NJ; ++j) {
-                        const uint4 wr = w[(g8 + r) * NJ + j];
-                        float2 wf[VEC / 2];
-                        if constexpr (DT == 1) {
-                            wf[0] = bf16x2_to_f32x2(wr.x);
-                            wf[1] = bf16x2_to_f32x2(wr.y);
-                            wf[2] = bf16x2_to_f32x2(wr.z);
-                            wf[3] = bf16x2_to_f32x2(wr.w);
-                        } else {
-                            wf[0] = make_float2(__uint_as_float(wr.x), __uint_as_float(wr.y));
-                            wf[1] = make_float2(__uint_as_float(wr.z), __uint_as_float(wr.w));
-                        }
-#pragma unroll
-                        for (int mm = 0; mm < MT; ++mm)
-#pragma unroll
-                            for (int e = 0; e < VEC / 2; ++e) acc[mm] = ffma2(wf[e], xv[mm][j][e], acc[mm]);
+                for (int j = 0; j < NJ; ++j) {
+                    const uint4 wr = w[(g8 + r) * NJ + j];
+                    float2 wf[VEC / 2];
+                    if constexpr (DT == 1) {
+                        wf[0] = bf16x2_to_f32x2(wr.x);
+                        wf[1] = bf16x2_to_f32x2(wr.y);
+                        wf[2] = bf16x2_to_f32x2(wr.z);
+                        wf[3] = bf16x2_to_f32x2(wr.w);
+                    } else {
+                        wf[0] = make_float2(__uint_as_float(wr.x), __uint_as_float(wr.y));
+                        wf[1] = make_float2(__uint_as_float(wr.z), __uint_as_float(wr.w));
                     }
 #pragma unroll
-                    for (int mm = 0; mm < MT; ++mm) part[mm][r] = acc[mm].x + acc[mm].y;
+                    for (int mm = 0; mm < MT; ++mm)
+#pragma unroll
+                        for (int e = 0; e < VEC / 2; ++e) acc[mm] = ffma2(wf[e], L.xv[mm][j][e], acc[mm]);
                 }
 #pragma unroll
-                for (int mm = 0; mm < MT; ++mm) {
-                    const float v = butterfly8(part[mm], lane);
-                    const int r = (lane >> 2) & 7;
-                    if ((lane & 3) == 0 && g8 + r < RB && b0 + g8 + r < lim)
-                        red[(warp * kRowsMaxRows + b0 + g8 + r) * MT + mm] = v;
+                for (int mm = 0; mm < MT; ++mm) part[mm][r] = acc[mm].x + acc[mm].y;
+            }
+#pragma unroll
+            for (int mm = 0; mm < MT; ++mm) {
+                const float v = butterfly8(part[mm], lane);
+                const int r = (lane >> 2) & 7;
+                if ((lane & 3) == 0 && g8 + r < RB && b0 + g8 + r < lim)
+                    red[(warp * kRowsMaxRows + b0 + g8 + r) * MT + mm] = v;
+            }
+        }
+    }
+
+    // Cross-warp sums of a segment's srows rows and the epilogue (after a block barrier).
+    __device__ static void epilogue(const GemvParams& p, Lane& L, int seg, int srows,
+                                    const float* red) {
+        const int tid = threadIdx.x, m = p.m;
+        const int rbase = L.row0 + seg;
+        if (p.epi == EPI_SWIGLU) {
+            for (int o = tid; o < (srows / 2) * m; o += kRowsThreads) {
+                const int pr = o / m, mm = o - pr * m;
+                float vg = 0.f, vu = 0.f;
+                for (int w = 0; w < kRowsWarps; ++w) {
+                    vg += red[(w * kRowsMaxRows + 2 * pr) * MT + mm];
+                    vu += red[(w * kRowsMaxRows + 2 * pr + 1) * MT + mm];
+                }
+                p.y[(size_t)mm * p.ldy + rbase / 2 + pr] = silu_f(vg) * vu;
+            }
+            return;
+        }
+        for (int o = tid; o < srows * m; o += kRowsThreads) {
+            const int r = o / m, mm = o - r * m;
+            float v = 0.f;
+            for (int w = 0; w < kRowsWarps; ++w) v += red[(w * kRowsMaxRows + r) * MT + mm];
+            const int row = rbase + r;
+            if constexpr (!kEpiPrefetch) {
+                if (p.bias) L.bias_v = p.bias[row];
+                if (p.epi == EPI_RESID) {
+                    L.res_v = __ldcg(p.res + (size_t)mm * p.ldres + row);
+                    if (p.ls) L.ls_v = __ldcg(p.ls + row);
                 }
             }
-        };
+            if (p.bias) v += L.bias_v;
+            float out;
+            if (p.epi == EPI_RESID) {
+                const float tt = p.ls ? L.ls_v * v : v;
+                out = L.res_v + tt;
+                if (p.tap) p.tap[(size_t)mm * p.ldtap + row] = out;
+            } else if (p.epi == EPI_GELU) {
+                out = gelu_f(v);
+            } else {
+                out = p.act == 1 ? silu_f(v) : v;
+            }
+            p.y[(size_t)mm * p.ldy + row] = out;
+        }
+    }
 
-        for (int seg = 0; seg < nrows; seg += kRowsMaxRows) {
-            const int srows = nrows - seg < kRowsMaxRows ? nrows - seg : kRowsMaxRows;
+    // everything after issue(): x and the norm prologue, the remaining batches, the epilogue.
+    // Every thread of the CTA calls it (block-wide barriers inside).
+    __device__ static void run(const GemvParams& p, int b, int P, uint4 (&wa)[BUF],
+                               uint4 (&wb)[BUF], float* sh) {
+        float* red = sh;  // [warps][kRowsMaxRows][MT]
+        Lane L;
+        setup(p, b, P, L);
+        const size_t row_bytes = (size_t)p.K * ES;
+        const char* Wb = static_cast<const char*>(p.W) + (size_t)L.row0 * row_bytes;
+        const uint64_t pol = l2_evict_first();
+        if (L.nrows > 0) fetch_epi(p, L, 0);
+        prologue(p, L, sh);
+
+        // ---- stream the rows, segment by segment, in double-buffered batches ------------------
+        for (int seg = 0; seg < L.nrows; seg += kRowsMaxRows) {
+            const int srows = L.nrows - seg < kRowsMaxRows ? L.nrows - seg : kRowsMaxRows;
             const char* Ws = Wb + (size_t)seg * row_bytes;
             if (seg > 0) {  // the first segment's first two batches came from issue()
                 load(p, Ws, row_bytes, 0, srows, pol, wa);
                 load(p, Ws, row_bytes, RB, srows, pol, wb);
-                fetch_epi(seg);
+                fetch_epi(p, L, seg);
             }
             // ping-pong: while one batch is consumed the other is in flight
             for (int b0 = 0; b0 < srows; b0 += 2 * RB) {
-                consume(wa, b0, srows);
+                consume(wa, b0, srows, L, red);
                 if (b0 + 2 * RB < srows) load(p, Ws, row_bytes, b0 + 2 * RB, srows, pol, wa);
-                if (b0 + RB < srows) consume(wb, b0 + RB, srows);
+                if (b0 + RB < srows) consume(wb, b0 + RB, srows, L, red);
                 if (b0 + 3 * RB < srows) load(p, Ws, row_bytes, b0 + 3 * RB, srows, pol, wb);
             }
             __syncthreads();
-
-            // ---- cross-warp sums and the epilogue ------------------------------------------------
-            const int rbase = row0 + seg;
-            if (p.epi == EPI_SWIGLU) {
-                for (int o = tid; o < (srows / 2) * m; o += kRowsThreads) {
-                    const int pr = o / m, mm = o - pr * m;
-                    float vg = 0.f, vu = 0.f;
-                    for (int w = 0; w < kRowsWarps; ++w) {
-                        vg += red[(w * kRowsMaxRows + 2 * pr) * MT + mm];
-                        vu += red[(w * kRowsMaxRows + 2 * pr + 1) * MT + mm];
-                    }
-                    p.y[(size_t)mm * p.ldy + rbase / 2 + pr] = silu_f(vg) * vu;
-                }
-            } else {
-                for (int o = tid; o < srows * m; o += kRowsThreads) {
-                    const int r = o / m, mm = o - r * m;
-                    float v = 0.f;
-                    for (int w = 0; w < kRowsWarps; ++w) v += red[(w * kRowsMaxRows + r) * MT + mm];
-                    const int row = rbase + r;
-                    if constexpr (!kEpiPrefetch) {
-                        if (p.bias) bias_v = p.bias[row];
-                        if (p.epi == EPI_RESID) {
-                            res_v = __ldcg(p.res + (size_t)mm * p.ldres + row);
-                            if (p.ls) ls_v = __ldcg(p.ls + row);
-                        }
-                    }
-                    if (p.bias) v += bias_v;
-                    float out;
-                    if (p.epi == EPI_RESID) {
-                        const float tt = p.ls ? ls_v * v : v;
-                        out = res_v + tt;
-                        if (p.tap) p.tap[(size_t)mm * p.ldtap + row] = out;
-                    } else if (p.epi == EPI_GELU) {
-                        out = gelu_f(v);
-                    } else {
-                        out = p.act == 1 ? silu_f(v) : v;
-                    }
-                    p.y[(size_t)mm * p.ldy + row] = out;
-                }
-            }
-            if (seg + kRowsMaxRows < nrows) __syncthreads();  // red is reused by the next segment
+            epilogue(p, L, seg, srows, red);
+            if (seg + kRowsMaxRows < L.nrows) __syncthreads();  // red is reused by the next segment
         }
     }
 };

@@ -127,15 +127,6 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
     return old;
 }
 
-// 1-D bulk copy global -> shared with an L2 policy (weights and cached K/V: evict_first)
-__device__ __forceinline__ void bulk_g2s_pol(uint32_t dst, const void* src, uint32_t bytes,
-                                             uint32_t bar, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;" ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-        : "memory");
-}
-
 // ---- waits and shared-memory loads of the hot loops ----------------------------------------------
 // try_wait with a suspend-time hint: a thread whose phase has not completed sleeps (up to the
 // hint) until it does, instead of spinning on the barrier and taking issue slots from the warps
