@@ -60,6 +60,13 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1 } dec_dtype;
                                   and K/V through a shared-memory ring while its consumer warps
                                   wait on tagged activations) instead of the chain of kernels;
                                   results agree within floating-point rounding */
+#define DEC_FLAG_TENSOR_GEMV 8u /* GEMVs of 3..8 rows over bf16 weights (steps of 3..8 streams,
+                                   prefill blocks) run on the tensor cores: tcgen05.mma with
+                                   TMEM accumulators, weight tiles by TMA, x split into three
+                                   bf16 terms (f32 accuracy); otherwise the FMA kernels serve
+                                   them.  Results agree within floating-point rounding.  On the
+                                   28-layer 2048-wide shapes it measured slower than the FMA
+                                   kernels, which stay the default */
 
 /*
  * Model geometry.  Talker fields follow the talker's Dims (Qwen3-TTS talker on wgpu, `Dims`

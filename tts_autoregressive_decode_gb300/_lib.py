@@ -17,7 +17,7 @@ STATUS_NAMES = {0: "DEC_OK", 1: "DEC_E_ARG", 2: "DEC_E_POS", 3: "DEC_E_CAPACITY"
                 4: "DEC_E_UNSUPPORTED", 5: "DEC_E_CUDA", 6: "DEC_E_DEVICE_CHECK"}
 DEC_QWEN3_TALKER, DEC_CODEC_WINDOWED = 0, 1
 DEC_F32, DEC_BF16 = 0, 1
-DEC_FLAG_TAPS, DEC_FLAG_NO_GRAPH, DEC_FLAG_PERSISTENT = 1, 2, 4
+DEC_FLAG_TAPS, DEC_FLAG_NO_GRAPH, DEC_FLAG_PERSISTENT, DEC_FLAG_TENSOR_GEMV = 1, 2, 4, 8
 
 # every symbol include/dec.h declares
 EXPORTS = ("dec_create", "dec_destroy", "dec_last_error", "dec_set_stream", "dec_prefill_kv",

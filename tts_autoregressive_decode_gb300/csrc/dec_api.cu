@@ -69,6 +69,8 @@ struct PlanEntry {
     cudaGraphNode_t io_node[3];       // multi-kernel plan: q/k/v GEMV, o-proj, final kernel
     cudaKernelNodeParams io_kp[3];    // their launch parameters
     GemvParams io_g[2];               // the two GEMVs' captured arguments
+    TmapBytes io_tm[2];               // ... and, for the tensor-core GEMV, its second argument
+    bool io_has_tm[2] = {false, false};
     FinalParams io_f;                 // the final kernel's captured arguments
 };
 
@@ -87,6 +89,7 @@ cudaError_t configure_kernels() {
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 64 && (done >> dev & 1u)) return cudaSuccess;
     if ((e = gemv_configure()) != cudaSuccess) return e;
+    if ((e = gemv_tc_configure()) != cudaSuccess) return e;
     if ((e = attention_configure()) != cudaSuccess) return e;
     if ((e = stream_configure()) != cudaSuccess) return e;
     if (dev < 64) done |= (uint64_t)1 << dev;
@@ -131,6 +134,10 @@ struct dec_ctx {
     int32_t* rope_axis = nullptr;  // [d/2] multimodal rope: the axis of each frequency
     float *xres = nullptr, *qkv = nullptr, *attn = nullptr, *act = nullptr;
     float *part = nullptr, *part_ml = nullptr;  // attention chunk partials
+    float* mpart = nullptr;       // tensor-core GEMV: partial sums of split tiles
+    size_t mpart_floats = 0;
+    unsigned* mtick = nullptr;    // ... and its tickets, one per 8-row tile
+    int mtick_n = 0;
     int32_t* len_dev = nullptr;
     unsigned* status = nullptr;
     int stall_phase = -1;   // dec_inject_stall: the next step's stalled phase and its poll bound
@@ -139,6 +146,8 @@ struct dec_ctx {
     float *io_in = nullptr, *io_out = nullptr;
     unsigned* status_host = nullptr;  // pinned
     std::vector<int> len_host;
+    std::vector<TmapBytes> tmaps;     // TMA descriptors of the GEMV matrices [layer][4] (bf16, > 2 rows)
+    std::vector<uint8_t> tmap_ok;     // ... and which of them were made
     std::vector<PlanEntry> plans;
     std::string err;
 };
@@ -261,6 +270,14 @@ bool stage_params(dec_ctx* ctx, int l, int stage, int m, const float* x_in, Gemv
     g.eps = c.norm_eps;
     g.status = ctx->status;
     g.unit = 1;
+    if (stage != 1 && !ctx->tmaps.empty()) {  // q/k/v, o-proj, gate/up, down: slots 0..3
+        const size_t slot = (size_t)l * 4 + (stage == 0 ? 0 : stage - 1);
+        g.tmap = ctx->tmap_ok[slot] ? ctx->tmaps[slot].b : nullptr;
+    }
+    g.mpart = ctx->mpart;
+    g.mpart_floats = ctx->mpart_floats;
+    g.mtick = ctx->mtick;
+    g.mtick_n = ctx->mtick_n;
     switch (stage) {
         case 0:  // norm + q/k/v
             g.W = talker ? W.qkv : W.in_proj;
@@ -597,8 +614,15 @@ cudaError_t record_io_nodes(PlanEntry& pe) {
         if (e != cudaSuccess) return e;
         if (!pe.io_kp[i].kernelParams || !pe.io_kp[i].kernelParams[0]) return cudaErrorInvalidValue;
     }
-    memcpy(&pe.io_g[0], pe.io_kp[0].kernelParams[0], sizeof(GemvParams));
-    memcpy(&pe.io_g[1], pe.io_kp[1].kernelParams[0], sizeof(GemvParams));
+    for (int i = 0; i < 2; ++i) {
+        memcpy(&pe.io_g[i], pe.io_kp[i].kernelParams[0], sizeof(GemvParams));
+        // the tensor-core GEMV takes its TMA descriptor as a second argument
+        pe.io_has_tm[i] = pe.io_kp[i].func == gemv_tc_kernel();
+        if (pe.io_has_tm[i]) {
+            if (!pe.io_kp[i].kernelParams[1]) return cudaErrorInvalidValue;
+            memcpy(&pe.io_tm[i], pe.io_kp[i].kernelParams[1], sizeof(TmapBytes));
+        }
+    }
     memcpy(&pe.io_f, pe.io_kp[2].kernelParams[0], sizeof(FinalParams));
     if (pe.io_g[0].x != pe.x_in || pe.io_g[1].res != pe.x_in || pe.io_f.out != pe.out)
         return cudaErrorInvalidValue;
@@ -612,8 +636,9 @@ cudaError_t update_io_nodes(PlanEntry& pe, const float* x_in, float* out) {
     g0.x = x_in;
     g1.res = x_in;
     f.out = out;
-    void* a0[] = {&g0};
-    void* a1[] = {&g1};
+    TmapBytes t0 = pe.io_tm[0], t1 = pe.io_tm[1];
+    void* a0[] = {&g0, &t0};  // the second entry only for the tensor-core GEMV
+    void* a1[] = {&g1, &t1};
     void* a2[] = {&f};
     void** args[3] = {a0, a1, a2};
     for (int i = 0; i < 3; ++i) {
@@ -1033,6 +1058,25 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     const size_t o_eos = take((size_t)S * 4);
     const size_t o_taps = (c.flags & DEC_FLAG_TAPS) ? take((size_t)c.layers * S * h * 4) : 0;
     const size_t o_in = take((size_t)S * h * 4), o_out = take((size_t)S * h * 4);
+    // tensor-core GEMV scratch (more than two rows): partial tiles of the CTAs and one ticket per
+    // 128-row tile
+    size_t o_mpart = 0, o_mtick = 0;
+    if (R > 2) {
+        const size_t shapes[4][2] = {{(size_t)ctx->qkv_rows, (size_t)h},
+                                     {(size_t)h, (size_t)qw},
+                                     {(size_t)(talker ? 2 * I : I), (size_t)h},
+                                     {(size_t)h, (size_t)I}};
+        size_t most = 0, rows = 0;
+        for (auto& sh : shapes) {
+            most = std::max(most, sh[0] * sh[1]);
+            rows = std::max(rows, sh[0]);
+        }
+        // the tensor-core GEMV: up to 16 partial tiles of 128 rows x 8 streams per CTA
+        ctx->mpart_floats = std::max(most / 32, (size_t)ctx->num_sms * 16 * 128 * 8);
+        ctx->mtick_n = (int)(rows / 8 + 1);
+        o_mpart = take(ctx->mpart_floats * 4);
+        o_mtick = take((size_t)ctx->mtick_n * 4);
+    }
     if ((e = cudaMalloc(&ctx->state, tot)) != cudaSuccess) return bail(cuda_fail(ctx, e, "state"));
     char* b = ctx->state;
     ctx->kc = reinterpret_cast<float*>(b + o_kc);
@@ -1053,6 +1097,10 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
     ctx->taps = (c.flags & DEC_FLAG_TAPS) ? reinterpret_cast<float*>(b + o_taps) : nullptr;
     ctx->io_in = reinterpret_cast<float*>(b + o_in);
     ctx->io_out = reinterpret_cast<float*>(b + o_out);
+    if (R > 2) {
+        ctx->mpart = reinterpret_cast<float*>(b + o_mpart);
+        ctx->mtick = reinterpret_cast<unsigned*>(b + o_mtick);  // zeroed with the state below
+    }
     // everything zero (K/V, scratch, lengths, status), then the stamps to empty
     if ((e = cudaMemsetAsync(ctx->state, 0, tot, s)) != cudaSuccess)
         return bail(cuda_fail(ctx, e, "state clear"));
@@ -1066,6 +1114,24 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* stream,
         (e = cudaMemcpyAsync(ctx->rope_sin, ts.data(), ts.size() * 4, cudaMemcpyHostToDevice, s)) !=
             cudaSuccess)
         return bail(cuda_fail(ctx, e, "rope tables"));
+    // TMA descriptors for the tensor-core GEMV (DEC_FLAG_TENSOR_GEMV: steps or prefill blocks of
+    // more than two rows over bf16 weights)
+    if ((c.flags & DEC_FLAG_TENSOR_GEMV) && R > 2 && c.weight_dtype == DEC_BF16) {
+        const size_t n = (size_t)c.layers * 4;
+        std::vector<TmapBytes> maps(n);
+        std::vector<uint8_t> ok(n, 0);
+        for (int l = 0; l < c.layers; ++l)
+            for (int st : {0, 2, 3, 4}) {
+                GemvParams g;
+                AttnParams a;
+                stage_params(ctx, l, st, R, ctx->io_in, g, a);
+                const size_t slot = (size_t)l * 4 + (st == 0 ? 0 : st - 1);
+                ok[slot] = gemv_tc_encode(g.W, g.N, g.K, maps[slot].b) == cudaSuccess;
+            }
+        (void)cudaGetLastError();  // a matrix the descriptors do not serve is not an error
+        ctx->tmaps.swap(maps);
+        ctx->tmap_ok.swap(ok);
+    }
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return bail(cuda_fail(ctx, e, "create sync"));
     *out = ctx;
     return DEC_OK;

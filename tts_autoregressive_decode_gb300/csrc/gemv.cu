@@ -338,6 +338,8 @@ cudaError_t launch_gemv(const GemvParams& p, int dtype, int num_sms, cudaStream_
     const int nj = rows_gemv_nj(p.K, p.m, dtype);
     // bias, SiLU and the modulate prologue are served by the split-K kernel only
     if (!nj && (p.bias || p.act || p.pro == PRO_LN_MOD)) return cudaErrorInvalidValue;
+    if (dtype == 1 && p.m > 2 && gemv_tc_ok(p, num_sms))  // 3..8 rows on the tensor cores
+        return launch_gemv_tc(p, num_sms, s, pdl);
     if (nj && p.m > 2) {  // 3..8 rows, one granule a lane
         if (dtype == 1) return p.m <= 4 ? launch_rows_t<1, 4, 1>(p, num_sms, s, pdl)
                                         : launch_rows_t<1, 8, 1>(p, num_sms, s, pdl);

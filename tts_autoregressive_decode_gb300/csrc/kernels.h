@@ -57,6 +57,15 @@ struct GemvParams {
     const float* bias;     // [N] or null (split-K GEMV, m <= 2, only)
     int act;               // EPI_STORE: 1 = SiLU
     const float* mod;      // PRO_LN_MOD: [2K] shift then scale
+    // tensor-core GEMV (3..8 rows, bf16 weights): the matrix's TMA descriptor (host memory,
+    // 128 bytes, copied into the launch's parameters; null: not served), partial sums of tiles
+    // split over CTAs and one ticket per 128-row tile (zero between launches)
+    const void* tmap;
+    float* mpart;
+    size_t mpart_floats;
+    unsigned* mtick;
+    int mtick_n;
+    int tc_stages, tc_cols, tc_band, tc_acc, tc_cb, tc_contrib;  // set by the launch
 };
 
 // dtype: 0 f32, 1 bf16.  Launches with the programmatic-dependency attribute when pdl.
@@ -65,6 +74,17 @@ constexpr int kGemvMaxSmem = 200 * 1024;
 cudaError_t launch_gemv(const GemvParams& p, int dtype, int num_sms, cudaStream_t s, bool pdl);
 cudaError_t gemv_configure();
 size_t gemv_smem_bytes(int m, int K);
+// the tensor-core GEMV: whether it serves this launch (bf16 weights with a TMA descriptor, 3..8
+// rows), its launch, and the descriptor of a row-major [N][K] bf16 matrix (128 bytes to out)
+bool gemv_tc_ok(const GemvParams& p, int num_sms);
+cudaError_t launch_gemv_tc(GemvParams p, int num_sms, cudaStream_t s, bool pdl);
+cudaError_t gemv_tc_configure();
+cudaError_t gemv_tc_encode(const void* W, int N, int K, void* out);
+const void* gemv_tc_kernel();  // the kernel's entry (graph nodes that launch it take two arguments)
+constexpr int kTmapBytes = 128;
+struct alignas(64) TmapBytes {  // one TMA descriptor, as the driver encodes it
+    unsigned char b[kTmapBytes];
+};
 
 // ---------------------------------------------------------------------------------------------
 // Split-K decode attention with the step's prologue fused in front of it.

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libttsdec.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["stream_step.cu", "gemv.cu", "attention.cu", "misc.cu", "dec_api.cu", "flow_api.cu",
+SOURCES = ["stream_step.cu", "gemv.cu", "gemv_tc.cu", "attention.cu", "misc.cu", "dec_api.cu", "flow_api.cu",
            "noalloc.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
