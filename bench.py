@@ -250,8 +250,8 @@ def bench_config(w: W.Workload, lengths, world: int) -> dict:
 
 
 def cpu_baselines(syn, seconds: float, one_core_seconds: float):
-    """The oracle timed twice on the host (SURVEY's plan): the sequential oracle on one core,
-    and the row-parallel build of the same oracle on every core (bitwise the same results)."""
+    """The oracle timed twice on the host: the sequential oracle on one core, and the
+    row-parallel build of the same oracle on every core (bitwise the same results)."""
     w = syn.workload
     threads = os.cpu_count() or 1
     n, dt = oracle_rate(syn, seconds, threads)

@@ -470,7 +470,7 @@ __device__ void merge_items(const AttnParams& p, int item0, int item_end, float*
     float* sm = scratch + (size_t)sub * 2 * p.max_chunks;
     float* sw = sm + p.max_chunks;
     const size_t base = ((size_t)r * p.H + hq) * p.max_chunks;
-    // round 1: this thread's first partial values and its share of the chunk statistics
+    // first load pass: this thread's first partial values and its share of the chunk statistics
     float v0[kMergeFirst];
 #pragma unroll
     for (int u = 0; u < kMergeFirst; ++u)
