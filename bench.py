@@ -65,6 +65,8 @@ def parse():
                    help="rows of the timed prefill block (talker workloads; 0: skip)")
     p.add_argument("--plan", choices=["kernels", "persistent"], default="kernels",
                    help="step plan: the chain of kernels (default) or the persistent kernel")
+    p.add_argument("--tensor-gemv", action="store_true",
+                   help="GEMVs of 3..8 rows (8-stream steps, prefill blocks) on the tensor cores")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--streams8", type=int, default=1,
                    help="also time the 8-stream 28-layer workload (1, default) or not (0)")
@@ -311,9 +313,11 @@ def time_streams8(args, stream, peak):
 
     from tts_autoregressive_decode_gb300.decoder import Decoder
 
+    from tts_autoregressive_decode_gb300 import _lib
+
     w = W.TALKER_H2048_L28_M8
     syn = W.generate(w)
-    dec = Decoder.from_synthetic(syn)
+    dec = Decoder.from_synthetic(syn, flags=_lib.DEC_FLAG_TENSOR_GEMV if args.tensor_gemv else 0)
     m, base = w.streams, list(syn.lengths)
     X = torch.from_numpy(syn.inputs).cuda()
     out = torch.empty((m, w.hidden), dtype=torch.float32, device="cuda")
@@ -383,7 +387,9 @@ def run_ours(args):
         syn.max_pos = max(syn.max_pos,
                           max(syn.lengths) + 2 * (args.warmup + args.steps) + 2 * w.steps + 8)
     from tts_autoregressive_decode_gb300 import _lib
-    dec = Decoder.from_synthetic(syn, flags=_lib.DEC_FLAG_PERSISTENT if args.plan == "persistent" else 0)
+    flags = (_lib.DEC_FLAG_PERSISTENT if args.plan == "persistent" else 0) | \
+        (_lib.DEC_FLAG_TENSOR_GEMV if args.tensor_gemv else 0)
+    dec = Decoder.from_synthetic(syn, flags=flags)
     m, h = w.streams, w.hidden
     base = list(syn.lengths)
     X = torch.from_numpy(syn.inputs).cuda()                  # [steps][m][h], resident in HBM
@@ -584,6 +590,8 @@ def run_ours(args):
     cfg = bench_config(w, base, world)
     plan = ("one CUDA graph per step holding one cooperative persistent kernel" if kpl == 1
             else f"one CUDA graph per step, {kpl} PDL-chained kernels")
+    if args.tensor_gemv:
+        plan += "; GEMVs of 3..8 rows (prefill blocks, 8-stream steps) on the tensor cores"
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

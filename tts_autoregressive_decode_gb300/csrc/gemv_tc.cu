@@ -31,6 +31,9 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "gemv_rows.cuh"
@@ -534,21 +537,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemv_tc(const GemvParams p,
                         most = nc[g4] > most ? nc[g4] : most;
                     }
                 }
-                for (int k = 0; k < most; ++k) {
-                    float4 a4[4], c4[4];
+                for (int k0 = 0; k0 < most; k0 += 2) {  // two holders of four tiles per load round
+                    float4 a4[2][4], c4[2][4];
 #pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4)
-                        if (k < nc[g4]) {
-                            const float* src = p.mpart + ((size_t)(blk[g4] + k) * kTcRows + r) * 8;
-                            a4[g4] = __ldcg(reinterpret_cast<const float4*>(src));
-                            c4[g4] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                        }
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4)
-                        if (k < nc[g4]) {
-                            yt[g4][0] += a4[g4].x; yt[g4][1] += a4[g4].y; yt[g4][2] += a4[g4].z; yt[g4][3] += a4[g4].w;
-                            yt[g4][4] += c4[g4].x; yt[g4][5] += c4[g4].y; yt[g4][6] += c4[g4].z; yt[g4][7] += c4[g4].w;
-                        }
+                        for (int g4 = 0; g4 < 4; ++g4)
+                            if (k0 + h < nc[g4]) {
+                                const float* src = p.mpart + ((size_t)(blk[g4] + k0 + h) * kTcRows + r) * 8;
+                                a4[h][g4] = __ldcg(reinterpret_cast<const float4*>(src));
+                                c4[h][g4] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                            }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)  // holder k0, then k0 + 1: the same order as one by one
+#pragma unroll
+                        for (int g4 = 0; g4 < 4; ++g4)
+                            if (k0 + h < nc[g4]) {
+                                float* y = yt[g4];
+                                y[0] += a4[h][g4].x; y[1] += a4[h][g4].y; y[2] += a4[h][g4].z; y[3] += a4[h][g4].w;
+                                y[4] += c4[h][g4].x; y[5] += c4[h][g4].y; y[6] += c4[h][g4].z; y[7] += c4[h][g4].w;
+                            }
                 }
 #pragma unroll
                 for (int g4 = 0; g4 < 4; ++g4)
@@ -640,6 +648,32 @@ static bool tc_plan(const GemvParams& p, int num_sms, TcPlan& pl) {
     if (p.pro != PRO_NONE && p.pro != PRO_RMS && p.nb && !a16(p.nb)) return false;
     if (p.pro == PRO_LN_MOD && (!a16(p.mod) || (p.K & 3))) return false;
     if (p.epi == EPI_SWIGLU && (p.N & 1)) return false;
+    // the search below takes tens of microseconds of host time: launches outside a CUDA graph
+    // (prefill blocks) reuse the plan of a shape seen before
+    struct Key {
+        int N, K, sms;
+        size_t mpart_floats;
+        int mtick_n;
+        bool scratch;
+    };
+    Key key;
+    memset(&key, 0, sizeof(key));  // padding included: keys compare bytewise
+    key.N = p.N;
+    key.K = p.K;
+    key.sms = num_sms;
+    key.mpart_floats = p.mpart_floats;
+    key.mtick_n = p.mtick_n;
+    key.scratch = p.mpart && p.mtick;
+    static std::mutex mu;
+    static std::vector<std::pair<Key, TcPlan>> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (auto& e : cache)
+            if (!memcmp(&e.first, &key, sizeof(Key))) {
+                pl = e.second;
+                return pl.grid > 0;
+            }
+    }
     bool found = false;
     for (int CB = 1; CB <= 4; CB *= 2) {
         if ((p.K / kTcChunk) % CB) continue;
@@ -654,6 +688,9 @@ static bool tc_plan(const GemvParams& p, int num_sms, TcPlan& pl) {
             }
         }
     }
+    if (!found) pl.grid = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 256) cache.push_back({key, pl});
     return found;
 }
 
