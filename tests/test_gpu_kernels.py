@@ -29,7 +29,7 @@ def _bf16(a):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("N,K", [(1, 8), (7, 24), (130, 392), (301, 1000), (4096, 2048),
                                  (2048, 6144), (1536, 512)])
-@pytest.mark.parametrize("m", [1, 2, 3, 8])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 7, 8])
 def test_gemv_matches_oracle(dec, dtype, N, K, m):
     rng = np.random.default_rng(N * 7 + K + m)
     Wf = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)

@@ -104,6 +104,13 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
     return pol;
 }
 
+// evict_normal: data read twice in a row by the same CTA (the first of two passes over rows)
+__device__ __forceinline__ uint64_t l2_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Order this thread's earlier generic-proxy accesses to shared memory before later async-proxy
 // (bulk copy) accesses: needed before a bulk copy overwrites shared memory that threads have read
 // or written since the previous copy.

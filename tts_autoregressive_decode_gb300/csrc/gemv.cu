@@ -249,10 +249,39 @@ __global__ void __launch_bounds__(kRowsThreads, MT <= 2 ? 2 : 1) k_gemv_rows(con
     __shared__ float sh[rows_smem_floats<MT>()];
     using R = RowsGemv<DT, MT, NJ, 8>;
     uint4 wa[8], wb[8];
-    R::issue(p, blockIdx.x, gridDim.x, wa, wb);
+    const uint64_t pol = l2_evict_first();
+    R::issue(p, blockIdx.x, gridDim.x, wa, wb, pol);
     pdl_trigger();
     pdl_wait();
-    R::run(p, blockIdx.x, gridDim.x, wa, wb, sh);
+    R::run(p, blockIdx.x, gridDim.x, wa, wb, sh, pol);
+}
+
+// 5..8 rows of a matrix wider than one granule a lane (the down GEMV, K = 6144): x of 8 rows
+// would take up to 192 registers a thread, so each CTA makes two passes over its rows, x rows
+// 0..3 and then 4..m-1.  The first pass reads the weights at normal L2 priority and the second,
+// which follows at once on the same CTA (a few hundred KB per CTA), finds them in L2: HBM sees
+// each weight once.  Rows of different passes write disjoint rows of y.
+template <int DT, int NJ>
+__global__ void __launch_bounds__(kRowsThreads, 1) k_gemv_rows2(const GemvParams p) {
+    __shared__ float sh[rows_smem_floats<4>()];
+    using R = RowsGemv<DT, 4, NJ, 8>;
+    uint4 wa[8], wb[8];
+    GemvParams q = p;
+    q.m = 4;
+    const uint64_t keep = l2_evict_normal();
+    R::issue(q, blockIdx.x, gridDim.x, wa, wb, keep);
+    pdl_trigger();
+    pdl_wait();
+    R::run(q, blockIdx.x, gridDim.x, wa, wb, sh, keep);
+    __syncthreads();  // the cross-warp scratch is reused
+    q.m = p.m - 4;
+    q.x = p.x + (size_t)4 * p.ldx;
+    q.y = p.y + (size_t)4 * p.ldy;
+    if (p.res) q.res = p.res + (size_t)4 * p.ldres;
+    if (p.tap) q.tap = p.tap + (size_t)4 * p.ldtap;
+    const uint64_t pol = l2_evict_first();
+    R::issue(q, blockIdx.x, gridDim.x, wa, wb, pol);
+    R::run(q, blockIdx.x, gridDim.x, wa, wb, sh, pol);
 }
 
 size_t gemv_smem_bytes(int m, int K) {
@@ -303,7 +332,8 @@ cudaError_t gemv_configure() {
 }
 
 template <int DT, int MT, int NJ>
-static cudaError_t launch_rows_t(GemvParams p, int num_sms, cudaStream_t s, bool pdl) {
+static cudaError_t launch_rows_t(GemvParams p, int num_sms, cudaStream_t s, bool pdl,
+                                 bool two_pass = false) {
     p.unit = p.epi == EPI_SWIGLU ? 2 : 1;
     const int units = p.N / p.unit;
     int grid = (p.per_sm > 0 ? p.per_sm : (MT <= 2 ? 2 : 1)) * num_sms;
@@ -321,6 +351,8 @@ static cudaError_t launch_rows_t(GemvParams p, int num_sms, cudaStream_t s, bool
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if constexpr (MT == 4 && NJ > 1)
+        if (two_pass) return cudaLaunchKernelEx(&cfg, k_gemv_rows2<DT, NJ>, p);
     return cudaLaunchKernelEx(&cfg, k_gemv_rows<DT, MT, NJ>, p);
 }
 
@@ -340,11 +372,18 @@ cudaError_t launch_gemv(const GemvParams& p, int dtype, int num_sms, cudaStream_
     if (!nj && (p.bias || p.act || p.pro == PRO_LN_MOD)) return cudaErrorInvalidValue;
     if (dtype == 1 && p.m > 2 && gemv_tc_ok(p, num_sms))  // 3..8 rows on the tensor cores
         return launch_gemv_tc(p, num_sms, s, pdl);
-    if (nj && p.m > 2) {  // 3..8 rows, one granule a lane
+    if (nj == 1 && p.m > 2) {  // 3..8 rows, one granule a lane
         if (dtype == 1) return p.m <= 4 ? launch_rows_t<1, 4, 1>(p, num_sms, s, pdl)
                                         : launch_rows_t<1, 8, 1>(p, num_sms, s, pdl);
         return p.m <= 4 ? launch_rows_t<0, 4, 1>(p, num_sms, s, pdl)
                         : launch_rows_t<0, 8, 1>(p, num_sms, s, pdl);
+    }
+    if (nj && p.m > 2) {  // 3..8 rows, 2..3 granules a lane: x of 4 rows at a time
+        const bool two = p.m > 4;
+        if (dtype == 1) return nj == 2 ? launch_rows_t<1, 4, 2>(p, num_sms, s, pdl, two)
+                                       : launch_rows_t<1, 4, 3>(p, num_sms, s, pdl, two);
+        return nj == 2 ? launch_rows_t<0, 4, 2>(p, num_sms, s, pdl, two)
+                       : launch_rows_t<0, 4, 3>(p, num_sms, s, pdl, two);
     }
     if (nj) {
         if (dtype == 1) return p.m <= 1 ? launch_rows_nj<1, 1>(p, nj, num_sms, s, pdl)

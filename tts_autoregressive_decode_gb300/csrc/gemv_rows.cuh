@@ -109,15 +109,14 @@ struct RowsGemv {
             }
     }
 
-    // the first two batches of CTA b's rows
+    // the first two batches of CTA b's rows (pol: the weights' L2 policy)
     __device__ static void issue(const GemvParams& p, int b, int P, uint4 (&wa)[BUF],
-                                 uint4 (&wb)[BUF]) {
+                                 uint4 (&wb)[BUF], uint64_t pol) {
         int row0, nrows;
         range(p, b, P, row0, nrows);
         const size_t row_bytes = (size_t)p.K * ES;
         const char* Wb = static_cast<const char*>(p.W) + (size_t)row0 * row_bytes;
         const int lim = nrows < kRowsMaxRows ? nrows : kRowsMaxRows;
-        const uint64_t pol = l2_evict_first();
         load(p, Wb, row_bytes, 0, lim, pol, wa);
         load(p, Wb, row_bytes, RB, lim, pol, wb);
     }
@@ -364,13 +363,12 @@ struct RowsGemv {
     // everything after issue(): x and the norm prologue, the remaining batches, the epilogue.
     // Every thread of the CTA calls it (block-wide barriers inside).
     __device__ static void run(const GemvParams& p, int b, int P, uint4 (&wa)[BUF],
-                               uint4 (&wb)[BUF], float* sh) {
+                               uint4 (&wb)[BUF], float* sh, uint64_t pol) {
         float* red = sh;  // [warps][kRowsMaxRows][MT]
         Lane L;
         setup(p, b, P, L);
         const size_t row_bytes = (size_t)p.K * ES;
         const char* Wb = static_cast<const char*>(p.W) + (size_t)L.row0 * row_bytes;
-        const uint64_t pol = l2_evict_first();
         if (L.nrows > 0) fetch_epi(p, L, 0);
         prologue(p, L, sh);
 
@@ -398,14 +396,16 @@ struct RowsGemv {
 };
 
 // granules per lane of the split-K GEMV for this shape (0: not served by it): up to 4 for
-// m <= 2; for 3..8 rows one granule (x of 8 rows then takes 64 registers a thread)
+// m <= 2; for 3..8 rows up to 3, x of at most 4 rows in registers at a time (4 rows x 3
+// granules: 96 registers a thread).  With one granule x holds all 8 rows (64 registers); wider
+// rows of 5..8 are two passes over the weights (k_gemv_rows2).
 inline int rows_gemv_nj(int K, int m, int dtype) {
     const int vec = dtype == 1 ? 8 : 4;
     const int per_pass = kRowsThreads * vec;  // elements one pass of the CTA covers
     const int nj = (K + per_pass - 1) / per_pass;
     if (nj < 1 || m < 1) return 0;
     if (m <= 2) return nj <= 4 ? nj : 0;
-    return (m <= 8 && nj == 1) ? 1 : 0;
+    return (m <= 8 && nj <= 3) ? nj : 0;
 }
 
 }  // namespace dec
