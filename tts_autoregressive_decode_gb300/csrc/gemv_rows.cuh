@@ -11,8 +11,9 @@
 // CTA's rows are streamed in batches of RB rows, the next batch's loads in flight while the
 // current one is consumed (two register buffers).  The caller issues the first two batches
 // (issue()) before it waits for x -- weights never depend on earlier work -- and run() does the
-// rest.  Per batch each warp folds its RB row partials across lanes with a transposed butterfly
-// (lanes 4r..4r+3 end up holding row r); the cross-warp sum and the epilogue run once per
+// rest.  Each warp folds 8 rows' partials at a time across lanes with a transposed butterfly
+// (lanes 4r..4r+3 end up holding row r): per batch of RB >= 8 rows, or, for one or two rows of x
+// and smaller batches, once per 8 / RB batches; the cross-warp sum and the epilogue run once per
 // segment of at most kRowsMaxRows rows.
 //
 // Activations (x, the residual) are read with ld.global.cg (L2): they were written by the
@@ -316,6 +317,56 @@ struct RowsGemv {
         }
     }
 
+    // Batches of fewer than 8 rows (one or two rows of x): the rows of 8 / RB consecutive batches (8 rows, alternating
+    // buffers, each refilled with the batch two ahead once consumed) share one transposed
+    // butterfly, instead of a butterfly per batch with most of its 8 rows empty.  Rows at or past
+    // lim compute on whatever the buffer holds and are not stored.
+    __device__ static void consume8(const GemvParams& p, const char* Ws, size_t row_bytes,
+                                    uint64_t pol, uint4 (&wa)[BUF], uint4 (&wb)[BUF], int b0,
+                                    int lim, const Lane& L, float* red) {
+        static_assert(RB < 8 && 8 % (2 * RB) == 0, "8 rows in pairs of batches");
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        float part[MT][8];
+#pragma unroll
+        for (int i = 0; i < 8 / RB; ++i) {
+            uint4(&w)[BUF] = (i & 1) ? wb : wa;
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                float2 acc[MT];
+#pragma unroll
+                for (int mm = 0; mm < MT; ++mm) acc[mm] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const uint4 wr = w[r * NJ + j];
+                    float2 wf[VEC / 2];
+                    if constexpr (DT == 1) {
+                        wf[0] = bf16x2_to_f32x2(wr.x);
+                        wf[1] = bf16x2_to_f32x2(wr.y);
+                        wf[2] = bf16x2_to_f32x2(wr.z);
+                        wf[3] = bf16x2_to_f32x2(wr.w);
+                    } else {
+                        wf[0] = make_float2(__uint_as_float(wr.x), __uint_as_float(wr.y));
+                        wf[1] = make_float2(__uint_as_float(wr.z), __uint_as_float(wr.w));
+                    }
+#pragma unroll
+                    for (int mm = 0; mm < MT; ++mm)
+#pragma unroll
+                        for (int e = 0; e < VEC / 2; ++e) acc[mm] = ffma2(wf[e], L.xv[mm][j][e], acc[mm]);
+                }
+#pragma unroll
+                for (int mm = 0; mm < MT; ++mm) part[mm][i * RB + r] = acc[mm].x + acc[mm].y;
+            }
+            const int next = b0 + i * RB + 2 * RB;  // the batch this buffer takes next
+            if (next < lim) load(p, Ws, row_bytes, next, lim, pol, w);
+        }
+#pragma unroll
+        for (int mm = 0; mm < MT; ++mm) {
+            const float v = butterfly8(part[mm], lane);
+            const int r = (lane >> 2) & 7;
+            if ((lane & 3) == 0 && b0 + r < lim) red[(warp * kRowsMaxRows + b0 + r) * MT + mm] = v;
+        }
+    }
+
     // Cross-warp sums of a segment's srows rows and the epilogue (after a block barrier).
     __device__ static void epilogue(const GemvParams& p, Lane& L, int seg, int srows,
                                     const float* red) {
@@ -382,11 +433,18 @@ struct RowsGemv {
                 fetch_epi(p, L, seg);
             }
             // ping-pong: while one batch is consumed the other is in flight
-            for (int b0 = 0; b0 < srows; b0 += 2 * RB) {
-                consume(wa, b0, srows, L, red);
-                if (b0 + 2 * RB < srows) load(p, Ws, row_bytes, b0 + 2 * RB, srows, pol, wa);
-                if (b0 + RB < srows) consume(wb, b0 + RB, srows, L, red);
-                if (b0 + 3 * RB < srows) load(p, Ws, row_bytes, b0 + 3 * RB, srows, pol, wb);
+            // (not with four granules, nor with x of 4 or 8 rows: the 8 rows' partials would stay
+            // live across the batches in a register file that is already full)
+            if constexpr (RB < 8 && NJ <= 3 && MT <= 2) {
+                for (int b0 = 0; b0 < srows; b0 += 8)
+                    consume8(p, Ws, row_bytes, pol, wa, wb, b0, srows, L, red);
+            } else {
+                for (int b0 = 0; b0 < srows; b0 += 2 * RB) {
+                    consume(wa, b0, srows, L, red);
+                    if (b0 + 2 * RB < srows) load(p, Ws, row_bytes, b0 + 2 * RB, srows, pol, wa);
+                    if (b0 + RB < srows) consume(wb, b0 + RB, srows, L, red);
+                    if (b0 + 3 * RB < srows) load(p, Ws, row_bytes, b0 + 3 * RB, srows, pol, wb);
+                }
             }
             __syncthreads();
             epilogue(p, L, seg, srows, red);
