@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # reports null until it is captured again.
 NCU_TRAFFIC = {
     # gate/up GEMV (k_gemv_rows<bf16, m1, NJ1>, N = 12288, K = 2048): one launch captured with
-    # ncu --set full on the 2-layer case of the same shapes; a launch does the same work at any
-    # layer count
-    W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_385_152, "source_sha": "79da7d0ccee7f346"},
+    # ncu (dram__bytes_read.sum, dram__bytes_write.sum) on the 2-layer case of the same shapes; a
+    # launch does the same work at any layer count
+    W.TALKER_H2048_L28.name: {"bytes_per_launch": 50_385_408, "source_sha": "6b44da6d6704a6bc"},
 }
 
 
