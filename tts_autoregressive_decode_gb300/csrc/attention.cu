@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(D) k_attn_merge(const AttnParams p) {
     __shared__ float scratch[2 * (kMaxSlots / kAttnChunk)];
     pdl_trigger();
     pdl_wait();
-    merge_items<D, D>(p, blockIdx.y * p.H + blockIdx.x, p.m * p.H, scratch);
+    merge_items<D, D, kMergeFirstWide>(p, blockIdx.y * p.H + blockIdx.x, p.m * p.H, scratch);
 }
 
 template <int D>

@@ -446,12 +446,14 @@ __device__ bool chunk_compute(const AttnParams& p, int r, int g, int c, const Ch
 // Merge of the chunk partials of NT / D (q head, stream) items at once, D threads per item:
 // items item0 .. min(item0 + NT/D, item_end) - 1 of the list r * H + hq.  Thread t of an item owns output
 // dimension t and sums the chunks in ascending order.  The chunk statistics and the first
-// kMergeFirst partial values are fetched in one round of independent loads.  `scratch` holds
+// FIRST partial values are fetched in one round of independent loads.  `scratch` holds
 // 2 * max_chunks floats per item.  All NT threads call it (block-wide barriers inside).
-constexpr int kMergeFirst = 48;  // partial rows of the first round (covers 3072 keys)
-constexpr int kMergeBatch = 16;  // partial rows per later round
+constexpr int kMergeFirst = 48;      // partial rows of the first round (covers 3072 keys) ...
+constexpr int kMergeFirstWide = 72;  // ... and in the stand-alone merge kernel (4608 keys), whose
+                                     // CTAs have registers to spare
+constexpr int kMergeBatch = 16;      // partial rows per later round
 
-template <int D, int NT>
+template <int D, int NT, int FIRST = kMergeFirst>
 __device__ void merge_items(const AttnParams& p, int item0, int item_end, float* scratch) {
     constexpr int CH = kAttnChunk;
     const int sub = threadIdx.x / D, t = threadIdx.x - sub * D;
@@ -471,9 +473,9 @@ __device__ void merge_items(const AttnParams& p, int item0, int item_end, float*
     float* sw = sm + p.max_chunks;
     const size_t base = ((size_t)r * p.H + hq) * p.max_chunks;
     // first load pass: this thread's first partial values and its share of the chunk statistics
-    float v0[kMergeFirst];
+    float v0[FIRST];
 #pragma unroll
-    for (int u = 0; u < kMergeFirst; ++u)
+    for (int u = 0; u < FIRST; ++u)
         v0[u] = u < nch ? __ldcg(p.part + (base + u) * D + t) : 0.f;
     float2 ml[(kMaxSlots / kAttnChunk + D - 1) / D];
 #pragma unroll
@@ -505,9 +507,9 @@ __device__ void merge_items(const AttnParams& p, int item0, int item_end, float*
     float den = 0.f, num = 0.f;
     for (int c = 0; c < nch; ++c) den += sw[c];
 #pragma unroll
-    for (int u = 0; u < kMergeFirst; ++u)
+    for (int u = 0; u < FIRST; ++u)
         if (u < nch) num += sm[u] * v0[u];
-    for (int c0 = kMergeFirst; c0 < nch; c0 += kMergeBatch) {
+    for (int c0 = FIRST; c0 < nch; c0 += kMergeBatch) {
         float v[kMergeBatch];
 #pragma unroll
         for (int u = 0; u < kMergeBatch; ++u)
