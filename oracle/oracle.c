@@ -31,7 +31,8 @@
  *   - multimodal rope (the talker's "interleaved MRoPE"): frequency i of the rotate_half table
  *     turns by the position of one of three axes (t, h, w), named by a per-frequency axis map
  *     the caller supplies (the pages give no section split); equal positions on all axes give
- *     the 1-D table (the pages' MRoPE-uniform identity)
+ *     the 1-D table (the pages' MRoPE-uniform identity).  The arithmetic for any map is pinned;
+ *     which split the real model uses is parity unpinned
  *   - rope tables: angle pos * theta^(-2i/d), cos/sin computed in double, rounded to orc_real
  *     (the talker's table builder is not printed; the codec computes the same angle in-kernel)
  *   - codec rope base 10000 (the value in rope_push_src)
